@@ -1,0 +1,224 @@
+/*
+ * dsa.h - C ABI of the B300 (sm_103a) DeepSeek Sparse Attention forward library.
+ *
+ * The forward pass has three steps, each a hand-written CUDA kernel:
+ *   1. lightning indexer  I[t,s] = sum_j w[t,j] * ReLU(q_I[t,j] . k_I[s])
+ *      ("DeepSeek V3.2: How Far Can Open Models Go If You Actually Try?",
+ *      §3.1, indexer equation; FP8, few heads);
+ *   2. fine-grained selection of the top-k positions of each row I[t,:]
+ *      (same §3.1; "Top-k operation" in the System Modules of "DeepSeek-V3.2:
+ *      Pushing the Frontier of Open Large Language Models"; k = 2048 in its Key
+ *      Hyperparameters);
+ *   3. MLA in MQA mode over the selected latent rows only:
+ *      u_t = Attn(h_t, {c_s : I[t,s] in Top-k(I[t,:])})  (same §3.1; §2.2 for
+ *      the shared latent K/V bank read by every head).
+ *
+ * Conventions shared by every entry point
+ *  - Ownership: every pointer is owned by the caller.  Tensors and workspace
+ *    are device memory of the current device; structs are host memory.  The
+ *    library allocates nothing, frees nothing and keeps no pointer after a
+ *    call returns.
+ *  - Layout: row-major and contiguous unless an ld (leading dimension, in
+ *    elements) is given.  Every tensor base pointer must be 16-byte aligned.
+ *  - Asynchrony: calls only enqueue work on `stream`; they return after host
+ *    validation and launch.  No call synchronises except
+ *    dsa_read_device_errors.
+ *  - Errors: host-side problems return a status before anything is enqueued;
+ *    launch failures return DSA_ERROR_LAUNCH.  Problems found on the device
+ *    (a bounded wait that ran out, an out-of-range selected index) set bits in
+ *    a per-device error word read by dsa_read_device_errors.
+ *    dsa_last_error_message() gives a one-line description of the last
+ *    non-success status returned on the calling host thread.
+ *  - Device: sm_103 (B300) only; other devices get DSA_ERROR_DEVICE.
+ *
+ * Batch geometry (ragged; prefill and decode use the same struct)
+ *  Sequence b has nq_b = cu_seqlens_q[b+1]-cu_seqlens_q[b] query tokens and
+ *  nkv_b = cu_seqlens_kv[b+1]-cu_seqlens_kv[b] cached tokens, nkv_b >= nq_b.
+ *  Query i of sequence b sits at position p = nkv_b - nq_b + i (bottom-right
+ *  aligned: prefill has nq = nkv, decode nq = 1) and its candidates are the
+ *  n = p + 1 keys s = 0..p of its own sequence (causal, self included).
+ *  Positions s are sequence-local; the global row of key s is
+ *  cu_seqlens_kv[b] + s.
+ */
+#ifndef DSA_H_
+#define DSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DSA_ABI_VERSION 1
+
+typedef enum {
+  DSA_SUCCESS = 0,
+  DSA_ERROR_INVALID_VALUE = 1,          /* bad pointer, size, alignment or struct field */
+  DSA_ERROR_NOT_SUPPORTED = 2,          /* valid but not implemented (dims/dtype combination) */
+  DSA_ERROR_INSUFFICIENT_WORKSPACE = 3, /* ws_bytes below the minimum of dsa_workspace_size */
+  DSA_ERROR_LAUNCH = 4,                 /* a CUDA launch or runtime call failed */
+  DSA_ERROR_DEVICE = 5,                 /* current device is not an sm_103 GPU */
+  DSA_ERROR_TIMEOUT = 6,                /* device error word: a bounded wait ran out */
+  DSA_ERROR_BAD_INDEX = 7               /* device error word: a selected index was out of range */
+} dsa_status_t;
+
+typedef enum {
+  DSA_DTYPE_F32 = 0,
+  DSA_DTYPE_BF16 = 1,
+  DSA_DTYPE_E4M3 = 2 /* OCP FP8 E4M3 ("fn": no infinities, 0x7F/0xFF are NaN) */
+} dsa_dtype_t;
+
+/* Bits of the per-device error word (dsa_read_device_errors). */
+#define DSA_DEVERR_TIMEOUT 0x1u   /* an mbarrier wait exceeded its time limit; the kernel gave up */
+#define DSA_DEVERR_BAD_INDEX 0x2u /* dsa_sparse_mla met an index outside [-1, n); it was skipped */
+
+/* Ragged batch.  cu_seqlens_* are device arrays of num_seqs+1 non-decreasing
+ * int32 offsets starting at 0.  The host fields must agree with them:
+ * max_seqlen_* >= every per-sequence length, total_* = last offset. */
+typedef struct {
+  int32_t num_seqs;
+  const int32_t* cu_seqlens_q;
+  const int32_t* cu_seqlens_kv;
+  int32_t max_seqlen_q;
+  int32_t max_seqlen_kv;
+  int64_t total_q;
+  int64_t total_kv;
+} dsa_batch_t;
+
+/* Lightning-indexer inputs.  The real-valued q_I / k_I are code * scale, one
+ * fp32 scale per query token (shared by its heads) and one per key row; NULL
+ * scale = 1.  Scales must be positive and finite.
+ *   q       [total_q, n_heads, head_dim]  dtype
+ *   q_scale [total_q] fp32 or NULL
+ *   k       [total_kv, head_dim]          dtype (one key per token, no head index)
+ *   k_scale [total_kv] fp32 or NULL
+ *   w       [total_q, n_heads] fp32       per-query head weights (any sign)
+ * E4M3 with (n_heads, head_dim) = (64, 128) runs on the tcgen05 tensor cores;
+ * other E4M3 / F32 shapes with n_heads <= 64 and head_dim <= 128 (head_dim a
+ * multiple of 16) run on a CUDA-core kernel. */
+typedef struct {
+  int32_t n_heads;
+  int32_t head_dim;
+  dsa_dtype_t dtype;
+  const void* q;
+  const float* q_scale;
+  const void* k;
+  const float* k_scale;
+  const float* w;
+} dsa_indexer_t;
+
+/* Sparse MLA (MQA mode) inputs.
+ *   q   [total_q, n_heads, d_qk]  dtype (queries absorbed into the latent space)
+ *   kv  [total_kv, d_qk]          dtype (one shared latent row per token; the
+ *                                 value is its first d_v columns)
+ * Scores are scale * (q . kv); softmax over the selected rows.
+ * BF16 with (n_heads, d_qk, d_v) = (128, 576, 512) runs on the tcgen05 tensor
+ * cores; other BF16 / F32 shapes with d_qk, d_v <= 1024 run on a CUDA-core
+ * kernel.  The output has the input dtype. */
+typedef struct {
+  int32_t n_heads;
+  int32_t d_qk;
+  int32_t d_v;
+  float scale;
+  dsa_dtype_t dtype;
+  const void* q;
+  const void* kv;
+} dsa_mla_t;
+
+/* Optional launch trace: the library records `events[count++]` (caller-created
+ * cudaEvents) before the first and after every kernel launch of a call, and
+ * stores in kernel_ids[i] the kernel launched between events[i] and
+ * events[i+1] (DSA_KERNEL_*).  Recording stops when capacity is reached. */
+enum {
+  DSA_KERNEL_INDEXER_TC = 1,
+  DSA_KERNEL_INDEXER_SIMT = 2,
+  DSA_KERNEL_TOPK = 3,
+  DSA_KERNEL_MLA_TC = 4,
+  DSA_KERNEL_MLA_SIMT = 5,
+  DSA_KERNEL_MLA_COMBINE = 6
+};
+typedef struct {
+  int32_t capacity; /* number of events[] (kernel_ids[] holds capacity-1) */
+  int32_t count;    /* events recorded so far; set to 0 before the call */
+  cudaEvent_t* events;
+  int32_t* kernel_ids;
+} dsa_trace_t;
+
+/* Workspace sizes (host only, no device access) for dsa_forward with the given
+ * batch, indexer and MLA description and top-k.  min_bytes: the least ws_bytes
+ * accepted; preferred_bytes: the size at which queries are processed in the
+ * largest chunks the library uses.  With indexer == NULL the sizes are those
+ * of dsa_sparse_mla alone.  Either output pointer may be NULL. */
+dsa_status_t dsa_workspace_size(const dsa_batch_t* batch, const dsa_indexer_t* indexer,
+                                const dsa_mla_t* mla, int32_t k, size_t* min_bytes,
+                                size_t* preferred_bytes);
+
+/* Step 1 alone.  Writes, for every query row r with n_r candidates,
+ * scores[r * ld_scores + s] = I[r, s] for s in [0, n_r) (fp32); columns >= n_r
+ * are not touched.  ld_scores >= max_seqlen_kv and a multiple of 4. */
+dsa_status_t dsa_index_scores(const dsa_batch_t* batch, const dsa_indexer_t* indexer,
+                              float* scores, int64_t ld_scores, cudaStream_t stream);
+
+/* Step 2 alone.  For every query row r, reads scores[r * ld_scores + s] for
+ * s in [0, n_r) and writes idx[r * k + i], i < k: the min(k, n_r) positions
+ * with the largest scores in ascending position order, then -1.  Ties go to
+ * the lower position and -0.0 equals +0.0 (NaN scores are outside the
+ * contract).  vals (nullable, [total_q, k] fp32) receives the selected scores
+ * (-inf in the -1 slots).  1 <= k <= 16384. */
+dsa_status_t dsa_topk(const dsa_batch_t* batch, const float* scores, int64_t ld_scores,
+                      int32_t k, int32_t* idx, float* vals, cudaStream_t stream);
+
+/* Step 3 alone.  For every query row r: softmax attention of its n_heads
+ * queries over the latent rows idx[r * k + i] (sequence-local positions; -1
+ * slots are skipped; entries outside [-1, n_r) are skipped and flag
+ * DSA_DEVERR_BAD_INDEX).  out [total_q, n_heads, d_v] (mla dtype);
+ * lse (nullable) [total_q, n_heads] fp32 natural-log sum of exp of the scaled
+ * scores (-inf and out = 0 for a row with nothing selected).  ws/ws_bytes:
+ * scratch for split-KV decode, sized by dsa_workspace_size(batch, NULL, mla,
+ * k, ...); may be NULL when that minimum is 0. */
+dsa_status_t dsa_sparse_mla(const dsa_batch_t* batch, const dsa_mla_t* mla, const int32_t* idx,
+                            int32_t k, void* out, float* lse, void* ws, size_t ws_bytes,
+                            cudaStream_t stream);
+
+/* The whole forward pass: steps 1-3 for every query row, processed in query
+ * chunks sized to ws_bytes.  out/lse as dsa_sparse_mla; idx_out (nullable)
+ * [total_q, k] receives the selected positions as dsa_topk writes them. */
+dsa_status_t dsa_forward(const dsa_batch_t* batch, const dsa_indexer_t* indexer,
+                         const dsa_mla_t* mla, int32_t k, void* out, float* lse,
+                         int32_t* idx_out, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* dsa_forward with an optional launch trace (trace may be NULL). */
+dsa_status_t dsa_forward_traced(const dsa_batch_t* batch, const dsa_indexer_t* indexer,
+                                const dsa_mla_t* mla, int32_t k, void* out, float* lse,
+                                int32_t* idx_out, void* ws, size_t ws_bytes,
+                                cudaStream_t stream, dsa_trace_t* trace);
+
+/* Synchronises `stream`, then reads and clears the current device's error word
+ * (DSA_DEVERR_* bits) into *flags.  Returns DSA_ERROR_TIMEOUT or
+ * DSA_ERROR_BAD_INDEX when the corresponding bit was set, else DSA_SUCCESS. */
+dsa_status_t dsa_read_device_errors(cudaStream_t stream, uint32_t* flags);
+
+/* Static description of a status code. */
+const char* dsa_status_string(dsa_status_t status);
+
+/* Detail of the last non-success status returned on this host thread. */
+const char* dsa_last_error_message(void);
+
+/* ABI version compiled into the library (DSA_ABI_VERSION). */
+int32_t dsa_abi_version(void);
+
+/* Test hook for the bounded-wait failure path.  The next tensor-core indexer
+ * launch of this process runs with the given mode: 1 = its producer skips the
+ * load of one key tile, so the MMA warp's wait runs out after its time limit
+ * (about 2 s), the kernel gives up cleanly and DSA_DEVERR_TIMEOUT is set.
+ * 0 = normal.  Not for production use. */
+void dsa_debug_inject_fault(uint32_t mode);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSA_H_ */

@@ -1,0 +1,544 @@
+// C ABI of the DSA forward library (declared in include/dsa.h): argument
+// validation, tensor-map encoding, launch configuration and the chunked
+// forward scheduler.  All kernels live in the headers included below; this is
+// the only translation unit of libdsa.so.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "dsa.h"
+#include "common.cuh"
+#include "indexer_tc.cuh"
+#include "mla_tc.cuh"
+#include "ptx.cuh"
+#include "simt.cuh"
+#include "topk.cuh"
+
+namespace {
+
+thread_local std::string g_last_msg;
+
+dsa_status_t fail(dsa_status_t st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_msg = buf;
+  return st;
+}
+
+#define DSA_TRY(expr)                          \
+  do {                                         \
+    const dsa_status_t st_ = (expr);           \
+    if (st_ != DSA_SUCCESS) return st_;        \
+  } while (0)
+
+// ---------------------------------------------------------------------------
+// Device facts, cached per device
+// ---------------------------------------------------------------------------
+constexpr int kMaxDevices = 64;
+struct DeviceInfo {
+  bool ready = false;
+  bool ok = false;
+  int sms = 0;
+  int smem_optin = 0;
+  bool attrs_set = false;
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+std::atomic<uint32_t> g_fault_next{0};
+
+dsa_status_t device_info(DeviceInfo** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return fail(DSA_ERROR_DEVICE, "no current CUDA device");
+  if (dev < 0 || dev >= kMaxDevices) return fail(DSA_ERROR_DEVICE, "device index %d out of range", dev);
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.ready) {
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    d.ok = (major == 10 && minor == 3);
+    d.ready = true;
+    if (!g_encode) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                           &q) == cudaSuccess &&
+          q == cudaDriverEntryPointSuccess)
+        g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+  }
+  if (!d.ok) return fail(DSA_ERROR_DEVICE, "device %d is not an sm_103 (B300) GPU", dev);
+  if (!g_encode) return fail(DSA_ERROR_DEVICE, "cuTensorMapEncodeTiled unavailable");
+  if (!d.attrs_set) {
+    if (cudaFuncSetAttribute(dsa::idx_tc::indexer_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             dsa::idx_tc::kSmemBytes) != cudaSuccess ||
+        cudaFuncSetAttribute(dsa::mla_tc::mla_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             dsa::mla_tc::kSmemBytes) != cudaSuccess)
+      return fail(DSA_ERROR_LAUNCH, "cudaFuncSetAttribute failed: %s",
+                  cudaGetErrorString(cudaGetLastError()));
+    d.attrs_set = true;
+  }
+  *out = &d;
+  return DSA_SUCCESS;
+}
+
+dsa_status_t encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner,
+                       uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = g_encode(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(DSA_ERROR_INVALID_VALUE, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return DSA_SUCCESS;
+}
+
+// ---------------------------------------------------------------------------
+// Launch trace
+// ---------------------------------------------------------------------------
+struct Tracer {
+  dsa_trace_t* t;
+  cudaStream_t s;
+  void begin() {
+    if (t && t->events && t->count == 0 && t->capacity > 0) cudaEventRecord(t->events[t->count++], s);
+  }
+  void after(int kernel_id) {
+    if (!t || !t->events || t->count <= 0 || t->count >= t->capacity) return;
+    if (t->kernel_ids) t->kernel_ids[t->count - 1] = kernel_id;
+    cudaEventRecord(t->events[t->count++], s);
+  }
+};
+
+dsa_status_t check_launch(const char* what) {
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(DSA_ERROR_LAUNCH, "%s launch failed: %s", what, cudaGetErrorString(e));
+  return DSA_SUCCESS;
+}
+
+// ---------------------------------------------------------------------------
+// Validation
+// ---------------------------------------------------------------------------
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+dsa_status_t check_batch(const dsa_batch_t* b) {
+  if (!b) return fail(DSA_ERROR_INVALID_VALUE, "batch is NULL");
+  if (b->num_seqs < 1) return fail(DSA_ERROR_INVALID_VALUE, "num_seqs must be >= 1 (got %d)", b->num_seqs);
+  if (!b->cu_seqlens_q || !b->cu_seqlens_kv) return fail(DSA_ERROR_INVALID_VALUE, "cu_seqlens pointer is NULL");
+  if (b->total_q < 0 || b->total_kv < 0 || b->total_kv < b->total_q)
+    return fail(DSA_ERROR_INVALID_VALUE, "totals must satisfy 0 <= total_q <= total_kv");
+  if (b->max_seqlen_q < 0 || b->max_seqlen_kv < b->max_seqlen_q)
+    return fail(DSA_ERROR_INVALID_VALUE, "max_seqlen_kv must be >= max_seqlen_q >= 0");
+  if (b->total_q > 0 && (b->max_seqlen_q < 1 || b->max_seqlen_kv < 1))
+    return fail(DSA_ERROR_INVALID_VALUE, "max_seqlen hints must be >= 1 for a non-empty batch");
+  if (b->total_kv >= (int64_t(1) << 31) || b->total_q >= (int64_t(1) << 24))
+    return fail(DSA_ERROR_NOT_SUPPORTED, "total_kv must be < 2^31 and total_q < 2^24");
+  return DSA_SUCCESS;
+}
+
+bool indexer_is_tc(const dsa_indexer_t* ix) {
+  return ix->dtype == DSA_DTYPE_E4M3 && ix->n_heads == dsa::idx_tc::kHeads &&
+         ix->head_dim == dsa::idx_tc::kDim;
+}
+
+dsa_status_t check_indexer(const dsa_indexer_t* ix) {
+  if (!ix) return fail(DSA_ERROR_INVALID_VALUE, "indexer is NULL");
+  if (!ix->q || !ix->k || !ix->w) return fail(DSA_ERROR_INVALID_VALUE, "indexer q, k and w are required");
+  if (!aligned16(ix->q) || !aligned16(ix->k) || !aligned16(ix->w) ||
+      (ix->q_scale && !aligned16(ix->q_scale)) || (ix->k_scale && !aligned16(ix->k_scale)))
+    return fail(DSA_ERROR_INVALID_VALUE, "indexer tensors must be 16-byte aligned");
+  if (ix->dtype != DSA_DTYPE_E4M3 && ix->dtype != DSA_DTYPE_F32)
+    return fail(DSA_ERROR_NOT_SUPPORTED, "indexer dtype must be E4M3 or F32");
+  if (ix->n_heads < 1 || ix->n_heads > dsa::simt::kMaxIdxHeads || ix->head_dim < 16 ||
+      ix->head_dim > dsa::simt::kMaxIdxDim || ix->head_dim % 16 != 0)
+    return fail(DSA_ERROR_NOT_SUPPORTED, "indexer needs 1 <= n_heads <= 64 and head_dim in {16, 32, ..., 128}");
+  return DSA_SUCCESS;
+}
+
+bool mla_is_tc(const dsa_mla_t* m) {
+  return m->dtype == DSA_DTYPE_BF16 && m->n_heads == dsa::mla_tc::kHeads && m->d_qk == dsa::mla_tc::kDqk &&
+         m->d_v == dsa::mla_tc::kDv;
+}
+
+dsa_status_t check_mla(const dsa_mla_t* m) {
+  if (!m) return fail(DSA_ERROR_INVALID_VALUE, "mla is NULL");
+  if (!m->q || !m->kv) return fail(DSA_ERROR_INVALID_VALUE, "mla q and kv are required");
+  if (!aligned16(m->q) || !aligned16(m->kv)) return fail(DSA_ERROR_INVALID_VALUE, "mla tensors must be 16-byte aligned");
+  if (m->dtype != DSA_DTYPE_BF16 && m->dtype != DSA_DTYPE_F32)
+    return fail(DSA_ERROR_NOT_SUPPORTED, "mla dtype must be BF16 or F32");
+  if (m->n_heads < 1 || m->d_qk < 1 || m->d_v < 1 || m->d_v > m->d_qk || m->d_qk > dsa::simt::kMaxMlaDim)
+    return fail(DSA_ERROR_NOT_SUPPORTED, "mla needs n_heads >= 1 and 1 <= d_v <= d_qk <= 1024");
+  if (!std::isfinite(m->scale)) return fail(DSA_ERROR_INVALID_VALUE, "mla scale must be finite");
+  return DSA_SUCCESS;
+}
+
+dsa_status_t check_k(int32_t k) {
+  if (k < 1 || k > 16384) return fail(DSA_ERROR_INVALID_VALUE, "k must be in [1, 16384] (got %d)", k);
+  return DSA_SUCCESS;
+}
+
+// ---------------------------------------------------------------------------
+// Per-step launchers over query rows [r0, r1).  Output/intermediate pointers
+// (scores, idx, vals, out, lse) already point at row r0.
+// ---------------------------------------------------------------------------
+dsa_status_t launch_index_scores(const DeviceInfo& dev, const dsa_batch_t* b, const dsa_indexer_t* ix,
+                                 float* scores, int64_t ld, int64_t r0, int64_t r1, cudaStream_t s,
+                                 Tracer& tr) {
+  const int64_t rows = r1 - r0;
+  if (rows <= 0) return DSA_SUCCESS;
+  if (indexer_is_tc(ix)) {
+    CUtensorMap tm_q, tm_k;
+    DSA_TRY(encode_2d(&tm_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, ix->q, dsa::idx_tc::kDim,
+                      static_cast<uint64_t>(b->total_q) * dsa::idx_tc::kHeads, dsa::idx_tc::kDim,
+                      dsa::idx_tc::kDim, dsa::idx_tc::kHeads));
+    DSA_TRY(encode_2d(&tm_k, CU_TENSOR_MAP_DATA_TYPE_UINT8, ix->k, dsa::idx_tc::kDim,
+                      static_cast<uint64_t>(b->total_kv), dsa::idx_tc::kDim, dsa::idx_tc::kDim,
+                      dsa::idx_tc::kKeys));
+    dsa::idx_tc::Params P{};
+    P.q_scale = ix->q_scale;
+    P.k_scale = ix->k_scale;
+    P.w = ix->w;
+    P.scores = scores;
+    P.ld = ld;
+    P.cu_q = b->cu_seqlens_q;
+    P.cu_kv = b->cu_seqlens_kv;
+    P.num_seqs = b->num_seqs;
+    P.row_begin = r0;
+    P.row_end = r1;
+    P.group = dsa::idx_tc::kMaxTokens;
+    P.fault = g_fault_next.exchange(0);
+    if (b->max_seqlen_q == 1) {
+      // decode: one token per sequence; split long key ranges so every SM works
+      const int64_t tiles = (b->total_kv + dsa::idx_tc::kKeys - 1) / dsa::idx_tc::kKeys + b->num_seqs;
+      const int64_t target = 4ll * dev.sms;
+      P.max_tiles = static_cast<int>(std::max<int64_t>(8, (tiles + target - 1) / target));
+    } else {
+      P.max_tiles = 1 << 24;
+    }
+    const int grid = dev.sms;
+    dsa::idx_tc::indexer_kernel<<<grid, dsa::idx_tc::kThreads, dsa::idx_tc::kSmemBytes, s>>>(tm_q, tm_k, P);
+    DSA_TRY(check_launch("indexer_tc"));
+    tr.after(DSA_KERNEL_INDEXER_TC);
+  } else {
+    if (rows > 65535) {
+      for (int64_t c = r0; c < r1; c += 65535) {
+        const int64_t e = std::min<int64_t>(r1, c + 65535);
+        DSA_TRY(launch_index_scores(dev, b, ix, scores + (c - r0) * ld, ld, c, e, s, tr));
+      }
+      return DSA_SUCCESS;
+    }
+    dim3 grid(static_cast<unsigned>((b->max_seqlen_kv + dsa::simt::kIdxThreads - 1) / dsa::simt::kIdxThreads),
+              static_cast<unsigned>(rows));
+    dsa::simt::indexer_kernel<<<grid, dsa::simt::kIdxThreads, 0, s>>>(
+        ix->q, ix->q_scale, ix->k, ix->k_scale, ix->w, ix->n_heads, ix->head_dim, ix->dtype,
+        scores, ld, b->cu_seqlens_q, b->cu_seqlens_kv, b->num_seqs, r0);
+    DSA_TRY(check_launch("indexer_simt"));
+    tr.after(DSA_KERNEL_INDEXER_SIMT);
+  }
+  return DSA_SUCCESS;
+}
+
+dsa_status_t launch_topk(const dsa_batch_t* b, const float* scores, int64_t ld, int32_t k, int32_t* idx,
+                         float* vals, int64_t r0, int64_t r1, cudaStream_t s, Tracer& tr) {
+  for (int64_t c = r0; c < r1; c += 2147483647ll) {
+    const int64_t e = std::min<int64_t>(r1, c + 2147483647ll);
+    dsa::topk::topk_kernel<<<static_cast<unsigned>(e - c), dsa::topk::kThreads, 0, s>>>(
+        scores + (c - r0) * ld, ld, k, idx + (c - r0) * k, vals ? vals + (c - r0) * k : nullptr,
+        b->cu_seqlens_q, b->cu_seqlens_kv, b->num_seqs, c);
+    DSA_TRY(check_launch("topk"));
+    tr.after(DSA_KERNEL_TOPK);
+  }
+  return DSA_SUCCESS;
+}
+
+// Split-KV plan for the tensor-core MLA kernel over `rows` query rows.
+struct MlaPlan {
+  int nsplit = 1;
+  int tiles_per_split = 1;
+  size_t ws_bytes = 0;
+};
+
+MlaPlan plan_mla(int sms, int64_t rows, int32_t k) {
+  MlaPlan p;
+  const int tiles = (k + dsa::mla_tc::kRows - 1) / dsa::mla_tc::kRows;
+  const int64_t clusters_wanted = std::max(1, sms / 2);
+  int want = 1;
+  if (rows < clusters_wanted) want = static_cast<int>((clusters_wanted + rows - 1) / rows);
+  want = std::min(want, tiles);
+  p.tiles_per_split = (tiles + want - 1) / want;
+  p.nsplit = (tiles + p.tiles_per_split - 1) / p.tiles_per_split;
+  if (p.nsplit > 1)
+    p.ws_bytes = static_cast<size_t>(rows) * p.nsplit * dsa::mla_tc::kHeads * (dsa::mla_tc::kDv + 1) * 4 + 256;
+  return p;
+}
+
+dsa_status_t launch_sparse_mla(const DeviceInfo& dev, const dsa_batch_t* b, const dsa_mla_t* m,
+                               const int32_t* idx, int32_t k, void* out, float* lse, void* ws,
+                               size_t ws_bytes, int64_t r0, int64_t r1, cudaStream_t s, Tracer& tr) {
+  const int64_t rows = r1 - r0;
+  if (rows <= 0) return DSA_SUCCESS;
+  if (mla_is_tc(m)) {
+    const MlaPlan plan = plan_mla(dev.sms, rows, k);
+    if (plan.ws_bytes > ws_bytes || (plan.ws_bytes > 0 && !ws))
+      return fail(DSA_ERROR_INSUFFICIENT_WORKSPACE, "sparse MLA needs %zu bytes of workspace, got %zu",
+                  plan.ws_bytes, ws_bytes);
+    if (ws && !aligned16(ws)) return fail(DSA_ERROR_INVALID_VALUE, "workspace must be 16-byte aligned");
+    CUtensorMap tm_q;
+    DSA_TRY(encode_2d(&tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, m->q, dsa::mla_tc::kDqk,
+                      static_cast<uint64_t>(b->total_q) * dsa::mla_tc::kHeads, dsa::mla_tc::kDqk * 2, 64,
+                      dsa::mla_tc::kHeads));
+    dsa::mla_tc::Params P{};
+    P.kv = static_cast<const __nv_bfloat16*>(m->kv);
+    P.idx = idx;
+    P.k = k;
+    P.c_log2 = m->scale * 1.4426950408889634f;
+    P.cu_q = b->cu_seqlens_q;
+    P.cu_kv = b->cu_seqlens_kv;
+    P.num_seqs = b->num_seqs;
+    P.row0 = r0;
+    P.nsplit = plan.nsplit;
+    P.tiles_per_split = plan.tiles_per_split;
+    P.out = static_cast<__nv_bfloat16*>(out);
+    P.lse = lse;
+    if (plan.nsplit > 1) {
+      P.part_o = static_cast<float*>(ws);
+      P.part_lse = reinterpret_cast<float*>(static_cast<char*>(ws) + static_cast<size_t>(rows) * plan.nsplit *
+                                                                        dsa::mla_tc::kHeads * dsa::mla_tc::kDv * 4);
+    }
+    const int64_t ctas = 2 * rows * plan.nsplit;
+    if (ctas > 2147483647ll) return fail(DSA_ERROR_NOT_SUPPORTED, "too many query rows in one call");
+    dsa::mla_tc::mla_kernel<<<static_cast<unsigned>(ctas), dsa::mla_tc::kThreads, dsa::mla_tc::kSmemBytes, s>>>(tm_q, P);
+    DSA_TRY(check_launch("mla_tc"));
+    tr.after(DSA_KERNEL_MLA_TC);
+    if (plan.nsplit > 1) {
+      dim3 grid(static_cast<unsigned>(rows), dsa::mla_tc::kHeads);
+      dsa::mla_tc::combine_kernel<<<grid, 128, 0, s>>>(P.part_o, P.part_lse, plan.nsplit, P.out, lse);
+      DSA_TRY(check_launch("mla_combine"));
+      tr.after(DSA_KERNEL_MLA_COMBINE);
+    }
+  } else {
+    for (int64_t c = r0; c < r1; c += 2147483647ll) {
+      const int64_t e = std::min<int64_t>(r1, c + 2147483647ll);
+      const size_t esz = m->dtype == DSA_DTYPE_BF16 ? 2 : 4;
+      dsa::simt::mla_kernel<<<static_cast<unsigned>(e - c), dsa::simt::kMlaWarps * 32, 0, s>>>(
+          m->q, m->kv, idx + (c - r0) * k, k, m->n_heads, m->d_qk, m->d_v, m->scale, m->dtype,
+          static_cast<char*>(out) + (c - r0) * m->n_heads * m->d_v * static_cast<int64_t>(esz),
+          lse ? lse + (c - r0) * m->n_heads : nullptr, b->cu_seqlens_q, b->cu_seqlens_kv, b->num_seqs, c);
+      DSA_TRY(check_launch("mla_simt"));
+      tr.after(DSA_KERNEL_MLA_SIMT);
+    }
+  }
+  return DSA_SUCCESS;
+}
+
+int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+
+// Forward workspace: [scores chunk | idx chunk | MLA split scratch]
+struct FwdPlan {
+  int64_t chunk;
+  int64_t ld;
+  size_t scores_bytes, idx_bytes, mla_bytes, total;
+};
+
+FwdPlan plan_forward(int sms, const dsa_batch_t* b, const dsa_mla_t* m, int32_t k, int64_t chunk) {
+  FwdPlan p;
+  p.chunk = std::max<int64_t>(1, std::min<int64_t>(chunk, b->total_q));
+  p.ld = round_up(std::max(1, b->max_seqlen_kv), 4);
+  p.scores_bytes = static_cast<size_t>(round_up(p.chunk * p.ld * 4, 256));
+  p.idx_bytes = static_cast<size_t>(round_up(p.chunk * static_cast<int64_t>(k) * 4, 256));
+  p.mla_bytes = 0;
+  if (m && mla_is_tc(m)) {
+    // the split plan is largest for the smallest row count
+    const int64_t nchunks = (b->total_q + p.chunk - 1) / p.chunk;
+    const int64_t last = std::max<int64_t>(1, b->total_q - (nchunks - 1) * p.chunk);
+    for (int64_t rows : {p.chunk, last})
+      p.mla_bytes = std::max(p.mla_bytes, plan_mla(sms, rows, k).ws_bytes);
+    p.mla_bytes = static_cast<size_t>(round_up(static_cast<int64_t>(p.mla_bytes), 256));
+  }
+  p.total = p.scores_bytes + p.idx_bytes + p.mla_bytes;
+  return p;
+}
+
+constexpr int64_t kPreferredChunk = 16384;
+constexpr int64_t kMinChunk = 64;
+
+int sms_for_sizing() {
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  return sms > 0 ? sms : 148;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t dsa_abi_version(void) { return DSA_ABI_VERSION; }
+
+const char* dsa_status_string(dsa_status_t s) {
+  switch (s) {
+    case DSA_SUCCESS: return "success";
+    case DSA_ERROR_INVALID_VALUE: return "invalid value";
+    case DSA_ERROR_NOT_SUPPORTED: return "not supported";
+    case DSA_ERROR_INSUFFICIENT_WORKSPACE: return "insufficient workspace";
+    case DSA_ERROR_LAUNCH: return "launch failure";
+    case DSA_ERROR_DEVICE: return "unsupported or missing device";
+    case DSA_ERROR_TIMEOUT: return "device wait timed out";
+    case DSA_ERROR_BAD_INDEX: return "selected index out of range";
+  }
+  return "unknown status";
+}
+
+const char* dsa_last_error_message(void) { return g_last_msg.c_str(); }
+
+dsa_status_t dsa_workspace_size(const dsa_batch_t* batch, const dsa_indexer_t* indexer, const dsa_mla_t* mla,
+                                int32_t k, size_t* min_bytes, size_t* preferred_bytes) {
+  DSA_TRY(check_batch(batch));
+  DSA_TRY(check_k(k));
+  if (mla) DSA_TRY(check_mla(mla));
+  const int sms = sms_for_sizing();
+  size_t mn = 0, pref = 0;
+  if (!indexer) {
+    if (mla && mla_is_tc(mla) && batch->total_q > 0) mn = pref = plan_mla(sms, batch->total_q, k).ws_bytes;
+  } else {
+    DSA_TRY(check_indexer(indexer));
+    if (batch->total_q > 0) {
+      mn = plan_forward(sms, batch, mla, k, kMinChunk).total;
+      pref = plan_forward(sms, batch, mla, k, kPreferredChunk).total;
+    }
+  }
+  if (min_bytes) *min_bytes = mn;
+  if (preferred_bytes) *preferred_bytes = std::max(mn, pref);
+  return DSA_SUCCESS;
+}
+
+dsa_status_t dsa_index_scores(const dsa_batch_t* batch, const dsa_indexer_t* indexer, float* scores,
+                              int64_t ld_scores, cudaStream_t stream) {
+  DSA_TRY(check_batch(batch));
+  DSA_TRY(check_indexer(indexer));
+  if (!scores || !aligned16(scores)) return fail(DSA_ERROR_INVALID_VALUE, "scores must be non-NULL and 16-byte aligned");
+  if (ld_scores < batch->max_seqlen_kv || ld_scores % 4 != 0)
+    return fail(DSA_ERROR_INVALID_VALUE, "ld_scores must be >= max_seqlen_kv and a multiple of 4");
+  DeviceInfo* dev;
+  DSA_TRY(device_info(&dev));
+  Tracer tr{nullptr, stream};
+  return launch_index_scores(*dev, batch, indexer, scores, ld_scores, 0, batch->total_q, stream, tr);
+}
+
+dsa_status_t dsa_topk(const dsa_batch_t* batch, const float* scores, int64_t ld_scores, int32_t k, int32_t* idx,
+                      float* vals, cudaStream_t stream) {
+  DSA_TRY(check_batch(batch));
+  DSA_TRY(check_k(k));
+  if (!scores || !aligned16(scores) || !idx || !aligned16(idx) || (vals && !aligned16(vals)))
+    return fail(DSA_ERROR_INVALID_VALUE, "scores and idx must be non-NULL and 16-byte aligned");
+  if (ld_scores < batch->max_seqlen_kv || ld_scores % 4 != 0)
+    return fail(DSA_ERROR_INVALID_VALUE, "ld_scores must be >= max_seqlen_kv and a multiple of 4");
+  DeviceInfo* dev;
+  DSA_TRY(device_info(&dev));
+  Tracer tr{nullptr, stream};
+  return launch_topk(batch, scores, ld_scores, k, idx, vals, 0, batch->total_q, stream, tr);
+}
+
+dsa_status_t dsa_sparse_mla(const dsa_batch_t* batch, const dsa_mla_t* mla, const int32_t* idx, int32_t k,
+                            void* out, float* lse, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  DSA_TRY(check_batch(batch));
+  DSA_TRY(check_mla(mla));
+  DSA_TRY(check_k(k));
+  if (!idx || !aligned16(idx) || !out || !aligned16(out) || (lse && !aligned16(lse)))
+    return fail(DSA_ERROR_INVALID_VALUE, "idx and out must be non-NULL and 16-byte aligned");
+  DeviceInfo* dev;
+  DSA_TRY(device_info(&dev));
+  Tracer tr{nullptr, stream};
+  return launch_sparse_mla(*dev, batch, mla, idx, k, out, lse, ws, ws_bytes, 0, batch->total_q, stream, tr);
+}
+
+dsa_status_t dsa_forward_traced(const dsa_batch_t* batch, const dsa_indexer_t* indexer, const dsa_mla_t* mla,
+                                int32_t k, void* out, float* lse, int32_t* idx_out, void* ws, size_t ws_bytes,
+                                cudaStream_t stream, dsa_trace_t* trace) {
+  DSA_TRY(check_batch(batch));
+  DSA_TRY(check_indexer(indexer));
+  DSA_TRY(check_mla(mla));
+  DSA_TRY(check_k(k));
+  if (!out || !aligned16(out) || (lse && !aligned16(lse)) || (idx_out && !aligned16(idx_out)))
+    return fail(DSA_ERROR_INVALID_VALUE, "out must be non-NULL; out, lse and idx_out 16-byte aligned");
+  if (ws && !aligned16(ws)) return fail(DSA_ERROR_INVALID_VALUE, "workspace must be 16-byte aligned");
+  DeviceInfo* dev;
+  DSA_TRY(device_info(&dev));
+  if (batch->total_q == 0) return DSA_SUCCESS;
+  // largest chunk that fits the workspace
+  const FwdPlan mn = plan_forward(dev->sms, batch, mla, k, kMinChunk);
+  if (!ws || ws_bytes < mn.total)
+    return fail(DSA_ERROR_INSUFFICIENT_WORKSPACE, "dsa_forward needs at least %zu bytes of workspace, got %zu",
+                mn.total, ws ? ws_bytes : 0);
+  int64_t lo = mn.chunk, hi = std::min<int64_t>(kPreferredChunk, batch->total_q);
+  while (lo < hi) {
+    const int64_t mid = (lo + hi + 1) / 2;
+    if (plan_forward(dev->sms, batch, mla, k, mid).total <= ws_bytes) lo = mid; else hi = mid - 1;
+  }
+  const FwdPlan plan = plan_forward(dev->sms, batch, mla, k, lo);
+  char* wsb = static_cast<char*>(ws);
+  float* scores = reinterpret_cast<float*>(wsb);
+  int32_t* idx_ws = reinterpret_cast<int32_t*>(wsb + plan.scores_bytes);
+  void* mla_ws = plan.mla_bytes ? wsb + plan.scores_bytes + plan.idx_bytes : nullptr;
+  const size_t esz = mla->dtype == DSA_DTYPE_BF16 ? 2 : 4;
+  Tracer tr{trace, stream};
+  tr.begin();
+  for (int64_t r0 = 0; r0 < batch->total_q; r0 += plan.chunk) {
+    const int64_t r1 = std::min<int64_t>(batch->total_q, r0 + plan.chunk);
+    int32_t* idx = idx_out ? idx_out + r0 * k : idx_ws;
+    DSA_TRY(launch_index_scores(*dev, batch, indexer, scores, plan.ld, r0, r1, stream, tr));
+    DSA_TRY(launch_topk(batch, scores, plan.ld, k, idx, nullptr, r0, r1, stream, tr));
+    DSA_TRY(launch_sparse_mla(*dev, batch, mla, idx, k,
+                              static_cast<char*>(out) + r0 * mla->n_heads * mla->d_v * static_cast<int64_t>(esz),
+                              lse ? lse + r0 * mla->n_heads : nullptr, mla_ws, plan.mla_bytes, r0, r1, stream, tr));
+  }
+  return DSA_SUCCESS;
+}
+
+dsa_status_t dsa_forward(const dsa_batch_t* batch, const dsa_indexer_t* indexer, const dsa_mla_t* mla, int32_t k,
+                         void* out, float* lse, int32_t* idx_out, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  return dsa_forward_traced(batch, indexer, mla, k, out, lse, idx_out, ws, ws_bytes, stream, nullptr);
+}
+
+dsa_status_t dsa_read_device_errors(cudaStream_t stream, uint32_t* flags) {
+  DeviceInfo* dev;
+  DSA_TRY(device_info(&dev));
+  if (cudaStreamSynchronize(stream) != cudaSuccess)
+    return fail(DSA_ERROR_LAUNCH, "stream synchronize failed: %s", cudaGetErrorString(cudaGetLastError()));
+  uint32_t v = 0;
+  const uint32_t zero = 0;
+  if (cudaMemcpyFromSymbol(&v, dsa::g_dev_errors, sizeof(v)) != cudaSuccess ||
+      cudaMemcpyToSymbol(dsa::g_dev_errors, &zero, sizeof(zero)) != cudaSuccess)
+    return fail(DSA_ERROR_LAUNCH, "reading the device error word failed: %s", cudaGetErrorString(cudaGetLastError()));
+  if (flags) *flags = v;
+  if (v & DSA_DEVERR_TIMEOUT) return fail(DSA_ERROR_TIMEOUT, "a device wait timed out (flags 0x%x)", v);
+  if (v & DSA_DEVERR_BAD_INDEX) return fail(DSA_ERROR_BAD_INDEX, "an index was out of range (flags 0x%x)", v);
+  return DSA_SUCCESS;
+}
+
+// Test hook: the next tensor-core indexer launch of this process runs with the
+// given fault mode (1 = its producer skips one key tile, so the MMA warp's
+// bounded wait runs out and the kernel reports DSA_DEVERR_TIMEOUT).
+void dsa_debug_inject_fault(uint32_t mode) { g_fault_next.store(mode); }
+
+}  // extern "C"

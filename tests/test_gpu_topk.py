@@ -1,0 +1,82 @@
+"""dsa_topk against the oracle's full-sort selection on identical fp32 score
+rows: index sets, their order and the returned values must be bit-exact."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sparse_long_context_07_b300 as dsa
+from tests.gpu_util import sample_rows
+
+pytestmark = pytest.mark.gpu
+
+
+def _cu(lens):
+    c = [0]
+    for x in lens:
+        c.append(c[-1] + x)
+    return torch.tensor(c, dtype=torch.int32, device="cuda")
+
+
+def _scores(T, ld, kind, seed):
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    if kind == "normal":
+        return torch.randn((T, ld), generator=g, device="cuda")
+    if kind == "ties":   # small integers: heavy ties, both signed zeros
+        s = torch.randint(-3, 4, (T, ld), generator=g, device="cuda").float()
+        neg = torch.rand((T, ld), generator=g, device="cuda") < 0.5
+        return torch.where((s == 0) & neg, torch.full_like(s, -0.0), s)
+    if kind == "const":
+        return torch.full((T, ld), 1.5, device="cuda")
+    raise ValueError(kind)
+
+
+def _check(batch, scores, ld, k, rows, n_of_row):
+    T = batch.total_q
+    idx = torch.full((T, k), -7, dtype=torch.int32, device="cuda")
+    vals = torch.full((T, k), float("nan"), device="cuda")
+    dsa.topk(batch, scores, ld, k, idx, vals)
+    torch.cuda.synchronize()
+    assert dsa.read_device_errors() == 0
+    S = scores.cpu().numpy()
+    I = idx.cpu().numpy()
+    V = vals.cpu().numpy()
+    for r in rows:
+        n = n_of_row[r]
+        ref = oracle.topk_indices(S[r, :n].astype(np.float64), k)
+        assert np.array_equal(I[r], ref), f"row {r} (n={n}, k={k})"
+        m = min(k, n)
+        assert np.array_equal(V[r, :m].view(np.uint32), S[r, ref[:m]].view(np.uint32)), f"vals row {r}"
+        assert np.all(np.isneginf(V[r, m:]))
+
+
+@pytest.mark.parametrize("kind", ["normal", "ties"])
+@pytest.mark.parametrize("k", [1, 64, 2048])
+def test_topk_prefill_rows(kind, k):
+    L = 5000
+    ld = L + 4
+    batch = dsa.Batch(_cu([L]), _cu([L]), [L], [L])
+    scores = _scores(L, ld, kind, seed=11 + k)
+    rows = sample_rows(L, 160, seed=k, must=[0, 1, k - 2, k - 1, k, k + 1, L - 1])
+    _check(batch, scores, ld, k, rows, {r: r + 1 for r in range(L)})
+
+
+def test_topk_long_decode_rows():
+    lens = [131072, 70001, 2049, 2048, 2047, 1, 5000, 100003]
+    k = 2048
+    ld = 131072
+    batch = dsa.Batch(_cu([1] * len(lens)), _cu(lens), [1] * len(lens), lens)
+    for kind in ("normal", "ties"):
+        scores = _scores(len(lens), ld, kind, seed=5)
+        _check(batch, scores, ld, k, range(len(lens)), dict(enumerate(lens)))
+
+
+def test_topk_all_equal_and_large_k():
+    lens = [20000, 16384, 16385, 3]
+    ld = 20000
+    batch = dsa.Batch(_cu([1] * 4), _cu(lens), [1] * 4, lens)
+    scores = _scores(4, ld, "const", seed=0)
+    _check(batch, scores, ld, 16384, range(4), dict(enumerate(lens)))
+    _check(batch, _scores(4, ld, "normal", seed=3), ld, 16384, range(4), dict(enumerate(lens)))
