@@ -1,0 +1,458 @@
+#!/usr/bin/env python
+"""Benchmark of the DSA forward pass (lightning indexer + top-k + sparse MLA).
+
+One step = one dsa_forward call over the whole workload (every query row
+through all three kernels).  Default workload: one 131072-token causal prefill
+(the 128K-context case), production dimensions, synthetic seeded inputs
+already resident in HBM.  Prints one JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
+
+Multi-GPU (torchrun): every rank runs an independent replica of the workload
+(independent sequences: no data-path collective); the step time is the max over
+ranks and the value is all ranks' tokens over that time.
+
+--impl reference times the fp64 CPU oracle (the reference implementation of
+this method) on the host cores, on an evenly spaced sample of query rows of the
+same workload per step, extrapolated to the workload's token rate.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "DSA fwd tokens/s (indexer+top-k+sparse MLA) at 128K ctx; % of HBM/FP8 roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--workload", default="prefill128k")
+    ap.add_argument("--e2e-steps", type=int, default=2)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target oracle time per sample")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------------------
+# algorithmic work of the workload (per query row: n = p+1 candidates)
+# ----------------------------------------------------------------------------
+def row_candidates(seqlens_q, seqlens_kv):
+    out = []
+    for nq, nkv in zip(seqlens_q, seqlens_kv):
+        out.append(np.arange(nkv - nq, nkv, dtype=np.int64) + 1)
+    return np.concatenate(out) if out else np.zeros(0, np.int64)
+
+
+def work_model(wl):
+    n = row_candidates(wl.seqlens_q, wl.seqlens_kv)
+    kk = np.minimum(n, wl.topk)
+    HI, dI, H = wl.n_idx_heads, wl.idx_dim, wl.n_heads
+    return {
+        "n": n,
+        # indexer: one H_I x d_I dot product per (query, candidate) pair
+        "indexer_flops": lambda rows: 2.0 * HI * dI * float(n[rows].sum()),
+        # sparse MLA: QK^T over d_qk and PV over d_v, per (query, head, selected row)
+        "mla_flops": lambda rows: 2.0 * H * (wl.d_qk + wl.d_v) * float(kk[rows].sum()),
+        # top-k: read each candidate score once, write k indices
+        "topk_bytes": lambda rows: 4.0 * float(n[rows].sum()) + 4.0 * wl.topk * len(n[rows]),
+        # sparse MLA bytes: gathered latent rows, Q, out, indices
+        "mla_bytes": lambda rows: float((kk[rows] * wl.d_qk * 2).sum()
+                                        + len(n[rows]) * (H * wl.d_qk * 2 + H * wl.d_v * 2 + wl.topk * 4)),
+    }
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def load_traffic():
+    """DRAM traffic per unit of work from the committed ncu summary, if any."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            return json.load(f)
+    except Exception:
+        return {}
+
+
+# ----------------------------------------------------------------------------
+# clocks during the timed region
+# ----------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = tempfile.mktemp(suffix=".csv")
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx = max(mx, float(parts[2]))
+                except ValueError:
+                    continue
+                for nm, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(nm)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------
+# oracle timing (cpu_baseline and the reference arm)
+# ----------------------------------------------------------------------------
+def oracle_sample(wl, target_s, seed=0):
+    """Time the fp64 oracle on evenly spaced query rows of the workload.
+    Returns (tokens/s extrapolated to the whole workload, description, threads)."""
+    import oracle
+    from tests.helpers import cu_np, idx_real, mla_real
+
+    cu_q, cu_kv = cu_np(wl)
+    _, pos, kv0, n = oracle.query_positions(cu_q, cu_kv)
+    T = len(n)
+    w_all = wl.w.float().cpu().numpy().astype(np.float64)
+    # decode of the key rows is per sequence, timed once and charged in full
+    t0 = time.perf_counter()
+    k_all = idx_real(wl, "k")
+    kv_dec = None
+    t_decode = time.perf_counter() - t0
+
+    def one(r):
+        q = idx_real(wl, "q", [r])[0]
+        I = oracle.index_scores_row(q, k_all[kv0[r]:kv0[r] + n[r]], w_all[r])
+        sel = oracle.topk_indices(I, wl.topk)
+        valid = sel[sel >= 0]
+        Q = mla_real(wl.Q, [r])[0]
+        kv = mla_real(wl.KV, kv0[r] + valid)
+        oracle.sparse_mla_row(Q, kv, np.arange(len(valid)), wl.scale, wl.d_v)
+
+    # probe the per-row cost on the middle row, then size the sample
+    t0 = time.perf_counter()
+    one(T // 2)
+    probe = time.perf_counter() - t0
+    R = int(max(4, min(T, target_s / max(probe, 1e-4))))
+    rows = np.unique(((np.arange(R) + 0.5) * T / R).astype(np.int64))
+    t0 = time.perf_counter()
+    for r in rows:
+        one(int(r))
+    el = time.perf_counter() - t0
+    per_row = el / len(rows)
+    total_s = t_decode + per_row * T
+    desc = (f"{len(rows)} evenly spaced query rows of {wl.name} (T={T}); per-row oracle time "
+            f"x T + one decode of the key cache, {el + t_decode:.1f} s measured")
+    del kv_dec
+    return T / total_s, desc, el + t_decode
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        th = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if th:
+            return int(max(th))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+# ----------------------------------------------------------------------------
+def main():
+    a = parse()
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl" if a.impl == "native" else "gloo")
+
+    import dsa_synth
+
+    if a.impl == "reference":
+        if rank != 0:
+            return
+        run_reference(a, world)
+        return
+
+    import sparse_long_context_07_b300 as dsa
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    # each rank owns an independent replica (its own seeded sequence)
+    wl = dsa_synth.WORKLOADS[a.workload](device=dev)
+    if world > 1 and rank > 0:
+        wl = reseed(wl, rank, dev)
+    b = dsa.Batch(wl.cu_q, wl.cu_kv, wl.seqlens_q, wl.seqlens_kv)
+    ix = dsa.Indexer(wl.q_idx, wl.k_idx, wl.w, wl.q_scale, wl.k_scale)
+    m = dsa.Mla(wl.Q, wl.KV, wl.scale, wl.d_v)
+    T = wl.total_q
+    k = wl.topk
+    out = torch.empty((T, wl.n_heads, wl.d_v), dtype=wl.Q.dtype, device=dev)
+    lse = torch.empty((T, wl.n_heads), dtype=torch.float32, device=dev)
+    _, pref = dsa.workspace_size(b, ix, m, k)
+    ws = torch.empty(pref, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(trace=None):
+        dsa.forward(b, ix, m, k, out, lse, None, ws, stream=stream, trace=trace)
+
+    for _ in range(max(3, a.warmup)):
+        step()
+    torch.cuda.synchronize()
+    if dsa.read_device_errors() != 0:
+        raise RuntimeError("device error word set during warm-up")
+
+    traces = [dsa.Trace(capacity=1024) for _ in range(a.steps)]
+    clocks = ClockSampler(local)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for i in range(a.steps):
+        step(traces[i])
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if world > 1:
+        dist.barrier()
+    ms = ev0.elapsed_time(ev1)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_per_step = ms / a.steps
+    tokens_per_step = T * world
+    value = tokens_per_step / (ms_per_step / 1e3)
+
+    # per-kernel durations from the launch trace
+    per_kernel = {}
+    launches = 0
+    for tr in traces:
+        for name, t in tr.launches():
+            d = per_kernel.setdefault(name, [0.0, 0])
+            d[0] += t
+            d[1] += 1
+            launches += 1
+    roof = roofline(wl, per_kernel, a.steps)
+
+    e2e = None
+    if not a.no_e2e:
+        e2e = measure_e2e(a, wl, dsa, b, ix, m, out, lse, ws, stream, world, dev)
+
+    if rank != 0:
+        return
+    cpu = None
+    if world == 1:
+        tps, desc, secs = oracle_sample(wl, a.cpu_seconds)
+        cpu = {"value": tps, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle", "sample": desc}
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": a.steps,
+        "warmup": max(3, a.warmup),
+        "ms_per_step": ms_per_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "e4m3+bf16",
+        "data": "synthetic",
+        "config": {"workload": wl.name, "seqlens_q": summarize(wl.seqlens_q),
+                   "seqlens_kv": summarize(wl.seqlens_kv), "topk": k,
+                   "indexer": f"{wl.n_idx_heads}x{wl.idx_dim} {wl.idx_dtype}",
+                   "mla": f"{wl.n_heads} heads d_qk={wl.d_qk} d_v={wl.d_v} {wl.mla_dtype}",
+                   "tokens_per_step": tokens_per_step,
+                   "l2": "inputs larger than L2 (no flush needed)", "parallelism": f"replicas x{world}"},
+        "roofline": roof,
+        "kernels_ms_per_step": {kname: v[0] / a.steps for kname, v in per_kernel.items()},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "clocks": clk,
+    }
+    print(json.dumps(line))
+
+
+def summarize(lens):
+    if len(set(lens)) == 1:
+        return f"{len(lens)}x{lens[0]}"
+    return f"{len(lens)} seqs, {min(lens)}..{max(lens)}, total {sum(lens)}"
+
+
+def reseed(wl, rank, dev):
+    import dsa_synth
+    return dsa_synth.make_workload(wl.name, wl.seqlens_q, wl.seqlens_kv, seed=1000 + rank, device=dev)
+
+
+def roofline(wl, per_kernel, steps):
+    """Roofline of the dominant kernel: algorithmic work of all its launches
+    over their total CUDA-event time, against the measured peak."""
+    if not per_kernel:
+        return None
+    peaks, src = load_peaks()
+    wm = work_model(wl)
+    allrows = np.arange(len(wm["n"]))
+    name = max(per_kernel, key=lambda kk: per_kernel[kk][0])
+    tot_ms, nl = per_kernel[name]
+    traffic_tab = load_traffic()
+    if name.startswith("indexer"):
+        work = wm["indexer_flops"](allrows) * steps
+        achieved = work / (tot_ms / 1e3) / 1e12
+        peak = 2.0 * peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
+        res = {"bound": "tensor", "unit": "TFLOP/s", "kernel": name,
+               "peak_note": f"e4m3 dense = 2 x {src} sustained bf16 cuBLAS"}
+    elif name.startswith("mla"):
+        work = wm["mla_flops"](allrows) * steps
+        achieved = work / (tot_ms / 1e3) / 1e12
+        peak = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
+        res = {"bound": "tensor", "unit": "TFLOP/s", "kernel": name, "peak_note": f"{src} sustained bf16 cuBLAS"}
+    else:
+        work = wm["topk_bytes"](allrows) * steps
+        achieved = work / (tot_ms / 1e3) / 1e9
+        peak = peaks.get("hbm_gbs")
+        res = {"bound": "hbm", "unit": "GB/s", "kernel": name, "peak_note": f"{src} copy bandwidth"}
+    tr = traffic_tab.get(name, {}).get(wl.name)
+    res.update({"achieved": achieved, "peak": peak, "frac": achieved / peak,
+                "traffic": (tr * nl / steps / max(1, nl / steps)) if tr else None,
+                "launches_per_step": nl / steps, "ms_per_step": tot_ms / steps})
+    return res
+
+
+def measure_e2e(a, wl, dsa, b, ix, m, out, lse, ws, stream, world, dev):
+    """Same metric end to end: pinned host inputs copied to the device, the
+    forward pass, and the output copied back, every step."""
+    import torch
+    srcs = [t for t in (wl.q_idx, wl.q_scale, wl.k_idx, wl.k_scale, wl.w, wl.Q, wl.KV) if t is not None]
+    host_in = [t.cpu().pin_memory() for t in srcs]
+    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    host_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = host_out.numel() * host_out.element_size() + host_lse.numel() * host_lse.element_size()
+
+    def step():
+        for h, d in zip(host_in, srcs):
+            d.copy_(h, non_blocking=True)
+        dsa.forward(b, ix, m, wl.topk, out, lse, None, ws, stream=stream)
+        host_out.copy_(out, non_blocking=True)
+        host_lse.copy_(lse, non_blocking=True)
+
+    step()
+    torch.cuda.synchronize()
+    n = max(1, a.e2e_steps)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(n):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    ms = ev0.elapsed_time(ev1) / n
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return {"value": wl.total_q * world / (ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": n}
+
+
+def run_reference(a, world):
+    """The fp64 oracle on the host cores, on the native arm's workload."""
+    import torch
+    import dsa_synth
+    # inputs are drawn on the GPU when there is one (generation is not timed);
+    # the oracle reads the rows it needs back to the host
+    gen_dev = "cuda" if torch.cuda.is_available() else "cpu"
+    wl = dsa_synth.WORKLOADS[a.workload](device=gen_dev)
+    for _ in range(max(0, a.warmup)):
+        pass  # the oracle has no state to warm up
+    vals, descs, secs = [], [], []
+    for i in range(a.steps):
+        tps, desc, s = oracle_sample(wl, max(1.0, a.cpu_seconds / max(1, a.steps)), seed=i)
+        vals.append(tps)
+        descs.append(desc)
+        secs.append(s)
+    value = statistics.median(vals)
+    cores = blas_threads()
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": value,
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": a.steps,
+        "warmup": a.warmup,
+        "ms_per_step": wl.total_q / value * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": wl.name, "seqlens_q": summarize(wl.seqlens_q),
+                   "seqlens_kv": summarize(wl.seqlens_kv), "topk": wl.topk},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": descs[0]},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

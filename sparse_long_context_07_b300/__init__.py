@@ -224,6 +224,9 @@ class Trace:
     def __init__(self, capacity: int = 512):
         import torch
         self.events = [torch.cuda.Event(enable_timing=True) for _ in range(capacity)]
+        for e in self.events:   # torch creates the CUDA event on first record
+            e.record()
+        torch.cuda.current_stream().synchronize()
         self._ev = (ctypes.c_void_p * capacity)(*[e.cuda_event for e in self.events])
         self._ids = (ctypes.c_int32 * capacity)()
         self.c = _Trace(capacity, 0, ctypes.cast(self._ev, ctypes.POINTER(ctypes.c_void_p)),

@@ -121,13 +121,26 @@ dsa_status_t encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base,
 struct Tracer {
   dsa_trace_t* t;
   cudaStream_t s;
-  void begin() {
-    if (t && t->events && t->count == 0 && t->capacity > 0) cudaEventRecord(t->events[t->count++], s);
+  bool broken = false;  // an event could not be recorded: stop tracing
+  void record() {
+    if (cudaEventRecord(t->events[t->count], s) != cudaSuccess) {
+      cudaGetLastError();  // do not leave a sticky error for the next launch check
+      broken = true;
+      return;
+    }
+    ++t->count;
+  }
+  dsa_status_t begin() {
+    if (t && t->events && t->count == 0 && t->capacity > 0) {
+      record();
+      if (broken) return fail(DSA_ERROR_INVALID_VALUE, "trace: cudaEventRecord failed on events[0]");
+    }
+    return DSA_SUCCESS;
   }
   void after(int kernel_id) {
-    if (!t || !t->events || t->count <= 0 || t->count >= t->capacity) return;
+    if (broken || !t || !t->events || t->count <= 0 || t->count >= t->capacity) return;
     if (t->kernel_ids) t->kernel_ids[t->count - 1] = kernel_id;
-    cudaEventRecord(t->events[t->count++], s);
+    record();
   }
 };
 
@@ -162,9 +175,11 @@ bool indexer_is_tc(const dsa_indexer_t* ix) {
          ix->head_dim == dsa::idx_tc::kDim;
 }
 
-dsa_status_t check_indexer(const dsa_indexer_t* ix) {
+// Tensor pointers may be NULL only when the batch has no rows to read.
+dsa_status_t check_indexer(const dsa_indexer_t* ix, const dsa_batch_t* b) {
   if (!ix) return fail(DSA_ERROR_INVALID_VALUE, "indexer is NULL");
-  if (!ix->q || !ix->k || !ix->w) return fail(DSA_ERROR_INVALID_VALUE, "indexer q, k and w are required");
+  if ((b->total_q > 0 && (!ix->q || !ix->w)) || (b->total_kv > 0 && !ix->k))
+    return fail(DSA_ERROR_INVALID_VALUE, "indexer q, k and w are required");
   if (!aligned16(ix->q) || !aligned16(ix->k) || !aligned16(ix->w) ||
       (ix->q_scale && !aligned16(ix->q_scale)) || (ix->k_scale && !aligned16(ix->k_scale)))
     return fail(DSA_ERROR_INVALID_VALUE, "indexer tensors must be 16-byte aligned");
@@ -181,9 +196,10 @@ bool mla_is_tc(const dsa_mla_t* m) {
          m->d_v == dsa::mla_tc::kDv;
 }
 
-dsa_status_t check_mla(const dsa_mla_t* m) {
+dsa_status_t check_mla(const dsa_mla_t* m, const dsa_batch_t* b) {
   if (!m) return fail(DSA_ERROR_INVALID_VALUE, "mla is NULL");
-  if (!m->q || !m->kv) return fail(DSA_ERROR_INVALID_VALUE, "mla q and kv are required");
+  if ((b->total_q > 0 && !m->q) || (b->total_kv > 0 && !m->kv))
+    return fail(DSA_ERROR_INVALID_VALUE, "mla q and kv are required");
   if (!aligned16(m->q) || !aligned16(m->kv)) return fail(DSA_ERROR_INVALID_VALUE, "mla tensors must be 16-byte aligned");
   if (m->dtype != DSA_DTYPE_BF16 && m->dtype != DSA_DTYPE_F32)
     return fail(DSA_ERROR_NOT_SUPPORTED, "mla dtype must be BF16 or F32");
@@ -415,13 +431,13 @@ dsa_status_t dsa_workspace_size(const dsa_batch_t* batch, const dsa_indexer_t* i
                                 int32_t k, size_t* min_bytes, size_t* preferred_bytes) {
   DSA_TRY(check_batch(batch));
   DSA_TRY(check_k(k));
-  if (mla) DSA_TRY(check_mla(mla));
+  if (mla) DSA_TRY(check_mla(mla, batch));
   const int sms = sms_for_sizing();
   size_t mn = 0, pref = 0;
   if (!indexer) {
     if (mla && mla_is_tc(mla) && batch->total_q > 0) mn = pref = plan_mla(sms, batch->total_q, k).ws_bytes;
   } else {
-    DSA_TRY(check_indexer(indexer));
+    DSA_TRY(check_indexer(indexer, batch));
     if (batch->total_q > 0) {
       mn = plan_forward(sms, batch, mla, k, kMinChunk).total;
       pref = plan_forward(sms, batch, mla, k, kPreferredChunk).total;
@@ -435,7 +451,8 @@ dsa_status_t dsa_workspace_size(const dsa_batch_t* batch, const dsa_indexer_t* i
 dsa_status_t dsa_index_scores(const dsa_batch_t* batch, const dsa_indexer_t* indexer, float* scores,
                               int64_t ld_scores, cudaStream_t stream) {
   DSA_TRY(check_batch(batch));
-  DSA_TRY(check_indexer(indexer));
+  DSA_TRY(check_indexer(indexer, batch));
+  if (batch->total_q == 0) return DSA_SUCCESS;
   if (!scores || !aligned16(scores)) return fail(DSA_ERROR_INVALID_VALUE, "scores must be non-NULL and 16-byte aligned");
   if (ld_scores < batch->max_seqlen_kv || ld_scores % 4 != 0)
     return fail(DSA_ERROR_INVALID_VALUE, "ld_scores must be >= max_seqlen_kv and a multiple of 4");
@@ -449,6 +466,7 @@ dsa_status_t dsa_topk(const dsa_batch_t* batch, const float* scores, int64_t ld_
                       float* vals, cudaStream_t stream) {
   DSA_TRY(check_batch(batch));
   DSA_TRY(check_k(k));
+  if (batch->total_q == 0) return DSA_SUCCESS;
   if (!scores || !aligned16(scores) || !idx || !aligned16(idx) || (vals && !aligned16(vals)))
     return fail(DSA_ERROR_INVALID_VALUE, "scores and idx must be non-NULL and 16-byte aligned");
   if (ld_scores < batch->max_seqlen_kv || ld_scores % 4 != 0)
@@ -462,8 +480,9 @@ dsa_status_t dsa_topk(const dsa_batch_t* batch, const float* scores, int64_t ld_
 dsa_status_t dsa_sparse_mla(const dsa_batch_t* batch, const dsa_mla_t* mla, const int32_t* idx, int32_t k,
                             void* out, float* lse, void* ws, size_t ws_bytes, cudaStream_t stream) {
   DSA_TRY(check_batch(batch));
-  DSA_TRY(check_mla(mla));
+  DSA_TRY(check_mla(mla, batch));
   DSA_TRY(check_k(k));
+  if (batch->total_q == 0) return DSA_SUCCESS;
   if (!idx || !aligned16(idx) || !out || !aligned16(out) || (lse && !aligned16(lse)))
     return fail(DSA_ERROR_INVALID_VALUE, "idx and out must be non-NULL and 16-byte aligned");
   DeviceInfo* dev;
@@ -476,10 +495,11 @@ dsa_status_t dsa_forward_traced(const dsa_batch_t* batch, const dsa_indexer_t* i
                                 int32_t k, void* out, float* lse, int32_t* idx_out, void* ws, size_t ws_bytes,
                                 cudaStream_t stream, dsa_trace_t* trace) {
   DSA_TRY(check_batch(batch));
-  DSA_TRY(check_indexer(indexer));
-  DSA_TRY(check_mla(mla));
+  DSA_TRY(check_indexer(indexer, batch));
+  DSA_TRY(check_mla(mla, batch));
   DSA_TRY(check_k(k));
-  if (!out || !aligned16(out) || (lse && !aligned16(lse)) || (idx_out && !aligned16(idx_out)))
+  if ((batch->total_q > 0 && !out) || !aligned16(out) || (lse && !aligned16(lse)) ||
+      (idx_out && !aligned16(idx_out)))
     return fail(DSA_ERROR_INVALID_VALUE, "out must be non-NULL; out, lse and idx_out 16-byte aligned");
   if (ws && !aligned16(ws)) return fail(DSA_ERROR_INVALID_VALUE, "workspace must be 16-byte aligned");
   DeviceInfo* dev;
@@ -502,7 +522,7 @@ dsa_status_t dsa_forward_traced(const dsa_batch_t* batch, const dsa_indexer_t* i
   void* mla_ws = plan.mla_bytes ? wsb + plan.scores_bytes + plan.idx_bytes : nullptr;
   const size_t esz = mla->dtype == DSA_DTYPE_BF16 ? 2 : 4;
   Tracer tr{trace, stream};
-  tr.begin();
+  DSA_TRY(tr.begin());
   for (int64_t r0 = 0; r0 < batch->total_q; r0 += plan.chunk) {
     const int64_t r1 = std::min<int64_t>(batch->total_q, r0 + plan.chunk);
     int32_t* idx = idx_out ? idx_out + r0 * k : idx_ws;

@@ -58,8 +58,10 @@ def test_mla_tc_decode_split_kv():
 
 
 def test_mla_tc_rescale_path():
-    # later latent rows are scaled up, so the running max of the scores keeps
-    # growing by more than the lazy-rescale threshold from tile to tile
+    # the rope columns (512..575, which take part in the scores but not in the
+    # value) of later latent rows are scaled up, so the running max of the
+    # scores keeps growing by more than the lazy-rescale threshold from tile to
+    # tile while the values stay N(0, 1)
     k = 1024
     wl = dsa_synth.make_workload("mla-resc", [1] * 2 + [400], [4096, 2500] + [400], n_idx_heads=16,
                                  idx_dim=32, idx_dtype="f32", device="cuda", seed=23)
@@ -67,8 +69,10 @@ def test_mla_tc_rescale_path():
     grow = torch.ones(S, device="cuda")
     for b in range(3):
         s0, s1 = int(wl.cu_kv[b]), int(wl.cu_kv[b + 1])
-        grow[s0:s1] = 1.0 + 2.0 * torch.arange(s1 - s0, device="cuda") / (s1 - s0)
-    wl.KV = (wl.KV.float() * grow[:, None]).to(torch.bfloat16)
+        grow[s0:s1] = 1.0 + 15.0 * torch.arange(s1 - s0, device="cuda") / (s1 - s0)
+    kv = wl.KV.float()
+    kv[:, wl.d_v:] *= grow[:, None]
+    wl.KV = kv.to(torch.bfloat16)
     idx = random_selection(wl, k, seed=4)
     out, lse = _run(wl, idx, k)
     assert dsa.read_device_errors() == 0
