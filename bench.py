@@ -47,6 +47,7 @@ def parse():
     ap.add_argument("--workload", default="prefill128k")
     ap.add_argument("--e2e-steps", type=int, default=2)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the oracle cpu_baseline leg")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target oracle time per sample")
     return ap.parse_args()
 
@@ -180,7 +181,9 @@ def oracle_sample(wl, target_s, seed=0):
         kv = mla_real(wl.KV, kv0[r] + valid)
         oracle.sparse_mla_row(Q, kv, np.arange(len(valid)), wl.scale, wl.d_v)
 
-    # probe the per-row cost on the middle row, then size the sample
+    # probe the per-row cost on the middle row (second, warm call), then size
+    # the sample
+    one(T // 2)
     t0 = time.perf_counter()
     one(T // 2)
     probe = time.perf_counter() - t0
@@ -299,7 +302,7 @@ def main():
     if rank != 0:
         return
     cpu = None
-    if world == 1:
+    if world == 1 and not a.no_cpu:
         tps, desc, secs = oracle_sample(wl, a.cpu_seconds)
         cpu = {"value": tps, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle", "sample": desc}
     line = {

@@ -12,6 +12,7 @@ Workloads (sizes and value distributions of the 128K-context DSA workloads):
               integer-grid variant with values in {-2..2}: seed 101)
   decode8k    4 sequences x 8192 cached tokens, 1 query each            (seed 2)
   prefill32k  one 32768-token causal prefill                             (seed 3)
+  prefill16k  one 16384-token causal prefill (profiling size)            (seed 6)
   ragged128k  64 decode sequences, context ~ U[16384, 131072], 10% of
               each sequence's keys planted toward its query             (seed 4)
   prefill128k one 131072-token causal prefill                            (seed 5)
@@ -229,6 +230,11 @@ def decode8k(device="cpu", grid=False):
     return make_workload("decode8k", [1] * 4, [8192] * 4, seed=2, grid=grid, device=device)
 
 
+def prefill16k(device="cpu", grid=False):
+    """One 16384-token causal prefill (a profiling-size case, inputs > L2)."""
+    return make_workload("prefill16k", [16384], [16384], seed=6, grid=grid, device=device)
+
+
 def prefill32k(device="cpu", grid=False):
     """One 32768-token causal prefill."""
     return make_workload("prefill32k", [32768], [32768], seed=3, grid=grid, device=device)
@@ -248,6 +254,7 @@ def prefill128k(device="cpu"):
 WORKLOADS = {
     "tiny": tiny,
     "decode8k": decode8k,
+    "prefill16k": prefill16k,
     "prefill32k": prefill32k,
     "ragged128k": ragged128k,
     "prefill128k": prefill128k,

@@ -295,18 +295,23 @@ struct MlaPlan {
   size_t ws_bytes = 0;
 };
 
-MlaPlan plan_mla(int sms, int64_t rows, int32_t k) {
-  MlaPlan p;
+// Fewer rows than half the SMs leave SMs idle, so each row's selected tiles
+// are split over several clusters (partials merged by the combine kernel).
+// The split count shrinks until its scratch fits `ws_cap` bytes.
+MlaPlan plan_mla(int sms, int64_t rows, int32_t k, size_t ws_cap = SIZE_MAX) {
   const int tiles = (k + dsa::mla_tc::kRows - 1) / dsa::mla_tc::kRows;
   const int64_t clusters_wanted = std::max(1, sms / 2);
   int want = 1;
   if (rows < clusters_wanted) want = static_cast<int>((clusters_wanted + rows - 1) / rows);
   want = std::min(want, tiles);
-  p.tiles_per_split = (tiles + want - 1) / want;
-  p.nsplit = (tiles + p.tiles_per_split - 1) / p.tiles_per_split;
-  if (p.nsplit > 1)
-    p.ws_bytes = static_cast<size_t>(rows) * p.nsplit * dsa::mla_tc::kHeads * (dsa::mla_tc::kDv + 1) * 4 + 256;
-  return p;
+  for (;; --want) {
+    MlaPlan p;
+    p.tiles_per_split = (tiles + want - 1) / want;
+    p.nsplit = (tiles + p.tiles_per_split - 1) / p.tiles_per_split;
+    if (p.nsplit > 1)
+      p.ws_bytes = static_cast<size_t>(rows) * p.nsplit * dsa::mla_tc::kHeads * (dsa::mla_tc::kDv + 1) * 4 + 256;
+    if (p.ws_bytes <= ws_cap || want <= 1) return p;
+  }
 }
 
 dsa_status_t launch_sparse_mla(const DeviceInfo& dev, const dsa_batch_t* b, const dsa_mla_t* m,
@@ -315,7 +320,7 @@ dsa_status_t launch_sparse_mla(const DeviceInfo& dev, const dsa_batch_t* b, cons
   const int64_t rows = r1 - r0;
   if (rows <= 0) return DSA_SUCCESS;
   if (mla_is_tc(m)) {
-    const MlaPlan plan = plan_mla(dev.sms, rows, k);
+    const MlaPlan plan = plan_mla(dev.sms, rows, k, ws ? ws_bytes : 0);
     if (plan.ws_bytes > ws_bytes || (plan.ws_bytes > 0 && !ws))
       return fail(DSA_ERROR_INSUFFICIENT_WORKSPACE, "sparse MLA needs %zu bytes of workspace, got %zu",
                   plan.ws_bytes, ws_bytes);
@@ -385,12 +390,9 @@ FwdPlan plan_forward(int sms, const dsa_batch_t* b, const dsa_mla_t* m, int32_t 
   p.idx_bytes = static_cast<size_t>(round_up(p.chunk * static_cast<int64_t>(k) * 4, 256));
   p.mla_bytes = 0;
   if (m && mla_is_tc(m)) {
-    // the split plan is largest for the smallest row count
-    const int64_t nchunks = (b->total_q + p.chunk - 1) / p.chunk;
-    const int64_t last = std::max<int64_t>(1, b->total_q - (nchunks - 1) * p.chunk);
-    for (int64_t rows : {p.chunk, last})
-      p.mla_bytes = std::max(p.mla_bytes, plan_mla(sms, rows, k).ws_bytes);
-    p.mla_bytes = static_cast<size_t>(round_up(static_cast<int64_t>(p.mla_bytes), 256));
+    // sized for a full chunk; a smaller tail chunk reduces its split count
+    // to fit (plan_mla with a cap)
+    p.mla_bytes = static_cast<size_t>(round_up(static_cast<int64_t>(plan_mla(sms, p.chunk, k).ws_bytes), 256));
   }
   p.total = p.scores_bytes + p.idx_bytes + p.mla_bytes;
   return p;
@@ -510,7 +512,9 @@ dsa_status_t dsa_forward_traced(const dsa_batch_t* batch, const dsa_indexer_t* i
   if (!ws || ws_bytes < mn.total)
     return fail(DSA_ERROR_INSUFFICIENT_WORKSPACE, "dsa_forward needs at least %zu bytes of workspace, got %zu",
                 mn.total, ws ? ws_bytes : 0);
+  // the preferred chunk when it fits, else the largest chunk that fits
   int64_t lo = mn.chunk, hi = std::min<int64_t>(kPreferredChunk, batch->total_q);
+  if (plan_forward(dev->sms, batch, mla, k, hi).total <= ws_bytes) lo = hi;
   while (lo < hi) {
     const int64_t mid = (lo + hi + 1) / 2;
     if (plan_forward(dev->sms, batch, mla, k, mid).total <= ws_bytes) lo = mid; else hi = mid - 1;

@@ -126,12 +126,44 @@ struct Walker {
   }
 };
 
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  uint64_t ra, rb, rc, rd;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(ra) : "f"(a.x), "f"(a.y));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(rb) : "f"(b.x), "f"(b.y));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(rc) : "f"(c.x), "f"(c.y));
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(rd) : "l"(ra), "l"(rb), "l"(rc));
+  float2 d;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(rd));
+  return d;
+}
+
+// acc += sum_j w[j] ReLU(x[j]) over 32 heads.  Even heads take ReLU as
+// max(x, 0) (ALU pipe), odd heads as x + |x| = 2 ReLU(x) (FMA pipe) against
+// weights staged at half value; both products then share one packed fp32x2
+// FMA.  Both forms are exact, so the sum equals the plain formula up to the
+// order of the additions.
+__device__ __forceinline__ void reduce_chunk(const uint32_t (&x)[32], const float* w, float2& acc) {
+  const float4* wv = reinterpret_cast<const float4*>(w);
+  float2 a2 = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const float4 wj = wv[j];
+    const float x0 = __uint_as_float(x[4 * j + 0]), x1 = __uint_as_float(x[4 * j + 1]);
+    const float x2 = __uint_as_float(x[4 * j + 2]), x3 = __uint_as_float(x[4 * j + 3]);
+    acc = ffma2(make_float2(wj.x, wj.y), make_float2(fmaxf(x0, 0.f), x1 + fabsf(x1)), acc);
+    a2 = ffma2(make_float2(wj.z, wj.w), make_float2(fmaxf(x2, 0.f), x3 + fabsf(x3)), a2);
+  }
+  acc.x += a2.x;
+  acc.y += a2.y;
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     indexer_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const Params P) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // 1024-byte aligned base, derived by pointer arithmetic on the shared array
+  // so that accesses through it stay shared-memory instructions
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(smem);
   float* wbuf = reinterpret_cast<float*>(smem + kOffW);
   const uint32_t bar0 = sbase + kOffBar;
@@ -254,7 +286,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int g = 2 * e + (et >> 6), j = et & 63;
         if (g < item.g) {
           const int64_t t = item.t0 + g;
-          wsm[g * kHeads + j] = __ldg(P.w + t * kHeads + j) * (P.q_scale ? __ldg(P.q_scale + t) : 1.f);
+          // odd heads are pre-halved: their ReLU is taken as x + |x| = 2 ReLU(x)
+          wsm[g * kHeads + j] = __ldg(P.w + t * kHeads + j) * (P.q_scale ? __ldg(P.q_scale + t) : 1.f) *
+                                ((j & 1) ? 0.5f : 1.f);
         }
       }
       mbar_arrive(w_full(e, qi & 1));
@@ -266,49 +300,45 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!warp_wait(acc_full(ab), (ti >> 1) & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
         // Columns of this warpgroup: token 2e at [0, 64), token 2e+1 at [64, 128)
-        // (relative to ta).  Stream them in 32-column chunks, loading chunk c+1
-        // before reducing chunk c.
+        // (relative to ta), read in 32-column chunks.
         const uint32_t ta = tmem + (static_cast<uint32_t>(wq * 32) << 16) + ab * kAccCols + e * 128;
         const int nchunk = ng >= 2 ? 4 : (ng == 1 ? 2 : 0);
         const int s = kt * kKeys + wq * 32 + lane;   // sequence-local key of this thread
         const int pmax = item.pos0 + item.g - 1;
         const float ks = (s <= pmax && P.k_scale) ? __ldg(P.k_scale + item.kv0 + s) : 1.f;
-        float acc[2] = {0.f, 0.f};
-        uint32_t xa[32], xb[32];
-        if (nchunk > 0) tmem_ld32(ta, xa);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          if (c >= nchunk) break;
-          tmem_wait_ld();
-          uint32_t (&cur)[32] = (c & 1) ? xb : xa;
-          uint32_t (&nxt)[32] = (c & 1) ? xa : xb;
-          if (c + 1 < nchunk) {
-            tmem_ld32(ta + 32 * (c + 1), nxt);
-          } else {
-            tc_fence_before();
-            mbar_arrive(acc_empty(ab));   // accumulator fully read: MMA may reuse it
-          }
-          const float4* wv = reinterpret_cast<const float4*>(wsm + (2 * e) * kHeads + 32 * c);
-          float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const float4 wj = wv[j];
-            a0 = fmaf(wj.x, fmaxf(__uint_as_float(cur[4 * j + 0]), 0.f), a0);
-            a1 = fmaf(wj.y, fmaxf(__uint_as_float(cur[4 * j + 1]), 0.f), a1);
-            a0 = fmaf(wj.z, fmaxf(__uint_as_float(cur[4 * j + 2]), 0.f), a0);
-            a1 = fmaf(wj.w, fmaxf(__uint_as_float(cur[4 * j + 3]), 0.f), a1);
-          }
-          acc[c >> 1] += a0 + a1;
-        }
-        if (nchunk == 0) {
+        // token 2e in chunks 0-1, token 2e+1 in chunks 2-3; chunk c+1 is loaded
+        // while chunk c is reduced
+        float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+        const float* wg = wsm + (2 * e) * kHeads;
+        auto release = [&]() {
           tc_fence_before();
-          mbar_arrive(acc_empty(ab));
+          mbar_arrive(acc_empty(ab));   // accumulator fully read: the MMA may reuse it
+        };
+        if (nchunk == 0) {
+          release();
+        } else {
+          uint32_t xa[32], xb[32];
+          tmem_ld32(ta, xa);
+          tmem_wait_ld();
+          tmem_ld32(ta + 32, xb);
+          reduce_chunk(xa, wg, acc[0]);
+          tmem_wait_ld();
+          if (nchunk == 4) tmem_ld32(ta + 64, xa); else release();
+          reduce_chunk(xb, wg + 32, acc[0]);
+          if (nchunk == 4) {
+            tmem_wait_ld();
+            tmem_ld32(ta + 96, xb);
+            reduce_chunk(xa, wg + 64, acc[1]);
+            tmem_wait_ld();
+            release();
+            reduce_chunk(xb, wg + 96, acc[1]);
+          }
         }
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
           const int g = 2 * e + u;
           if (u < ng && s <= item.pos0 + g)
-            P.scores[(item.t0 + g - P.row_begin) * P.ld + s] = acc[u] * ks;
+            P.scores[(item.t0 + g - P.row_begin) * P.ld + s] = (acc[u].x + acc[u].y) * ks;
         }
       }
     }
