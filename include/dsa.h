@@ -183,6 +183,28 @@ dsa_status_t dsa_sparse_mla(const dsa_batch_t* batch, const dsa_mla_t* mla, cons
                             int32_t k, void* out, float* lse, void* ws, size_t ws_bytes,
                             cudaStream_t stream);
 
+/* Scratch-free variant of dsa_sparse_mla.  The pages have no counterpart: this
+ * is an integration aid.  It is for callers that cannot hand the library a
+ * device workspace, for example a plugin whose host runtime owns every device
+ * allocation and offers no scratch buffer, or a serving loop that reserved
+ * all device memory up front and may not call cudaMalloc in the middle of a
+ * step (the call can fail, or synchronise the device).  Same arguments,
+ * results and errors as dsa_sparse_mla, minus ws/ws_bytes: the split-KV
+ * partials of small decode batches live in a 24 MiB array compiled into the
+ * library, which every GPU that loads the library holds until the process
+ * exits.  A batch whose split plan needs more than 24 MiB (decode batches of
+ * roughly 21 to 73 query rows) is rejected with DSA_ERROR_NOT_SUPPORTED;
+ * call dsa_sparse_mla with a workspace for those.  The first call on each
+ * device looks up the array's device address (cudaGetSymbolAddress), so make
+ * that first call before any stream capture.  Every call shares the one
+ * array and it keeps the last call's contents; the kernels overwrite
+ * everything they read from it, so nothing needs clearing, but calls that
+ * overlap on the GPU (other streams, other host threads) race on it and must
+ * be serialised by the caller. */
+dsa_status_t dsa_sparse_mla_noalloc(const dsa_batch_t* batch, const dsa_mla_t* mla,
+                                    const int32_t* idx, int32_t k, void* out, float* lse,
+                                    cudaStream_t stream);
+
 /* The whole forward pass: steps 1-3 for every query row, processed in query
  * chunks sized to ws_bytes.  out/lse as dsa_sparse_mla; idx_out (nullable)
  * [total_q, k] receives the selected positions as dsa_topk writes them. */

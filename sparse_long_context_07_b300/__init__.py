@@ -79,6 +79,7 @@ _sig = {
     "dsa_index_scores": (ctypes.c_int, [_P, _P, _P, ctypes.c_int64, _P]),
     "dsa_topk": (ctypes.c_int, [_P, _P, ctypes.c_int64, ctypes.c_int32, _P, _P, _P]),
     "dsa_sparse_mla": (ctypes.c_int, [_P, _P, _P, ctypes.c_int32, _P, _P, _P, ctypes.c_size_t, _P]),
+    "dsa_sparse_mla_noalloc": (ctypes.c_int, [_P, _P, _P, ctypes.c_int32, _P, _P, _P]),
     "dsa_forward": (ctypes.c_int, [_P, _P, _P, ctypes.c_int32, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "dsa_forward_traced": (ctypes.c_int, [_P, _P, _P, ctypes.c_int32, _P, _P, _P, _P, ctypes.c_size_t,
                                           _P, _P]),
@@ -216,6 +217,15 @@ def sparse_mla(batch: Batch, mla: Mla, idx, k: int, out, lse=None, ws=None, stre
     nbytes = 0 if ws is None else ws.numel() * ws.element_size()
     _check(lib().dsa_sparse_mla(_ref(batch), _ref(mla), _ptr(idx), int(k), _ptr(out), _ptr(lse), _ptr(ws),
                                nbytes, _stream(stream)), "dsa_sparse_mla")
+
+
+def sparse_mla_noalloc(batch: Batch, mla: Mla, idx, k: int, out, lse=None, stream=None):
+    """dsa_sparse_mla without a workspace argument, for callers that cannot
+    allocate device scratch: its split-KV partials live in a fixed 24 MiB array
+    inside the library (shared by all calls; overlapping calls race).  Batches
+    needing more than that raise DSAError (ERROR_NOT_SUPPORTED)."""
+    _check(lib().dsa_sparse_mla_noalloc(_ref(batch), _ref(mla), _ptr(idx), int(k), _ptr(out), _ptr(lse),
+                                        _stream(stream)), "dsa_sparse_mla_noalloc")
 
 
 class Trace:

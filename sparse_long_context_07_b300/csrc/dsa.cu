@@ -407,6 +407,43 @@ int sms_for_sizing() {
   return sms > 0 ? sms : 148;
 }
 
+// ---------------------------------------------------------------------------
+// Built-in scratch for dsa_sparse_mla_noalloc
+// ---------------------------------------------------------------------------
+constexpr size_t kStaticScratchBytes = size_t(24) << 20;  // 24 MiB
+
+}  // namespace
+
+// Split-KV partials of dsa_sparse_mla_noalloc.  Every GPU that loads the
+// library holds this array until the process exits.  Host code must not pass
+// the symbol itself to a kernel (on the host it is only a stand-in): the
+// device address comes from cudaGetSymbolAddress, looked up once per device.
+static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
+
+namespace {
+
+void* g_static_scratch_addr[kMaxDevices] = {};
+std::mutex g_static_scratch_mu;
+
+// Device address of g_static_scratch on the current device (first call per
+// device does the lookup).
+dsa_status_t static_scratch_address(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+    return fail(DSA_ERROR_DEVICE, "no usable current CUDA device");
+  std::lock_guard<std::mutex> lk(g_static_scratch_mu);
+  if (!g_static_scratch_addr[dev]) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
+    if (e != cudaSuccess || !p)
+      return fail(DSA_ERROR_LAUNCH, "cudaGetSymbolAddress of the built-in scratch failed: %s",
+                  cudaGetErrorString(e));
+    g_static_scratch_addr[dev] = p;
+  }
+  *out = g_static_scratch_addr[dev];
+  return DSA_SUCCESS;
+}
+
 }  // namespace
 
 extern "C" {
@@ -491,6 +528,30 @@ dsa_status_t dsa_sparse_mla(const dsa_batch_t* batch, const dsa_mla_t* mla, cons
   DSA_TRY(device_info(&dev));
   Tracer tr{nullptr, stream};
   return launch_sparse_mla(*dev, batch, mla, idx, k, out, lse, ws, ws_bytes, 0, batch->total_q, stream, tr);
+}
+
+dsa_status_t dsa_sparse_mla_noalloc(const dsa_batch_t* batch, const dsa_mla_t* mla, const int32_t* idx,
+                                    int32_t k, void* out, float* lse, cudaStream_t stream) {
+  DSA_TRY(check_batch(batch));
+  DSA_TRY(check_mla(mla, batch));
+  DSA_TRY(check_k(k));
+  if (batch->total_q == 0) return DSA_SUCCESS;
+  if (!idx || !aligned16(idx) || !out || !aligned16(out) || (lse && !aligned16(lse)))
+    return fail(DSA_ERROR_INVALID_VALUE, "idx and out must be non-NULL and 16-byte aligned");
+  DeviceInfo* dev;
+  DSA_TRY(device_info(&dev));
+  // the same split plan dsa_sparse_mla would use with an unlimited workspace
+  const size_t need = mla_is_tc(mla) ? plan_mla(dev->sms, batch->total_q, k).ws_bytes : 0;
+  if (need > kStaticScratchBytes)
+    return fail(DSA_ERROR_NOT_SUPPORTED,
+                "dsa_sparse_mla_noalloc: this batch needs %zu bytes of split-KV scratch but the built-in "
+                "scratch holds %zu bytes; call dsa_sparse_mla with a workspace instead",
+                need, kStaticScratchBytes);
+  void* scratch = nullptr;
+  DSA_TRY(static_scratch_address(&scratch));
+  Tracer tr{nullptr, stream};
+  return launch_sparse_mla(*dev, batch, mla, idx, k, out, lse, scratch, kStaticScratchBytes, 0,
+                           batch->total_q, stream, tr);
 }
 
 dsa_status_t dsa_forward_traced(const dsa_batch_t* batch, const dsa_indexer_t* indexer, const dsa_mla_t* mla,
