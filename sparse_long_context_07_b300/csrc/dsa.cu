@@ -295,14 +295,16 @@ struct MlaPlan {
   size_t ws_bytes = 0;
 };
 
-// Fewer rows than half the SMs leave SMs idle, so each row's selected tiles
-// are split over several clusters (partials merged by the combine kernel).
+// Each (row, split) unit runs on two CTAs (one per half of the output
+// columns).  Fewer units than half the SMs leave SMs idle, so each row's
+// selected tiles are then split over several units (partials merged by the
+// combine kernel).
 // The split count shrinks until its scratch fits `ws_cap` bytes.
 MlaPlan plan_mla(int sms, int64_t rows, int32_t k, size_t ws_cap = SIZE_MAX) {
   const int tiles = (k + dsa::mla_tc::kRows - 1) / dsa::mla_tc::kRows;
-  const int64_t clusters_wanted = std::max(1, sms / 2);
+  const int64_t units_wanted = std::max(1, sms / 2);
   int want = 1;
-  if (rows < clusters_wanted) want = static_cast<int>((clusters_wanted + rows - 1) / rows);
+  if (rows < units_wanted) want = static_cast<int>((units_wanted + rows - 1) / rows);
   want = std::min(want, tiles);
   for (;; --want) {
     MlaPlan p;
@@ -330,6 +332,7 @@ dsa_status_t launch_sparse_mla(const DeviceInfo& dev, const dsa_batch_t* b, cons
                       static_cast<uint64_t>(b->total_q) * dsa::mla_tc::kHeads, dsa::mla_tc::kDqk * 2, 64,
                       dsa::mla_tc::kHeads));
     dsa::mla_tc::Params P{};
+    P.q = static_cast<const __nv_bfloat16*>(m->q);
     P.kv = static_cast<const __nv_bfloat16*>(m->kv);
     P.idx = idx;
     P.k = k;

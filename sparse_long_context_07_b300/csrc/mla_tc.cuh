@@ -6,32 +6,40 @@
 // MQA mode, one shared latent row per token read by all heads, §3.1 and §2.2).
 // Dimensions: 128 heads, d_qk = 576, d_v = 512, bf16 in, fp32 accumulate.
 //
-// The fp32 output accumulator of one query token (128 heads x 512) fills the
-// whole TMEM of an SM (128 lanes x 512 columns), leaving no room for the score
-// tile.  So a cluster of two CTAs (two SMs) serves one token:
-//   CTA r holds Q[:, 288r : 288r+288] and gathers the same columns of each
-//   selected latent row, computes the partial scores S_r = Q_r K_r^T
-//   (M = 128 heads, N = 64 rows, K = 288), and the two CTAs swap S_r through
-//   distributed shared memory.  Both then hold S = S_0 + S_1 bit-identically
-//   (fp32 addition commutes), run the same online softmax, and CTA r
-//   accumulates O[:, 256r : 256r+256] += P V_r (M = 128, N = 256, K = 64) in
-//   its TMEM (256 columns + 2 x 64 for S).
-// Each latent row is fetched once per cluster (640 B per CTA, the 64 columns
-// 256..319 by both), so all 128 heads share one gather (the MQA saving).
+// The fp32 output of one query token (128 heads x 512) would fill the whole
+// TMEM of an SM, so two CTAs serve each token: CTA `half` owns the output
+// columns [256 half, 256 half + 256).  Both CTAs compute the full score tile
+// S = Q K^T over all 576 columns themselves, so they never exchange data
+// (shared memory of another SM is far too slow for a per-tile exchange on
+// this part); the price is that the Q K^T products are done twice.
 //
-// Warp roles per CTA (320 threads):
-//   warps 0-3  softmax / epilogue, thread h = head h = TMEM lane h
-//   warps 4-7  gather: cp.async 16 B chunks of the selected rows into a
-//              128-byte-swizzled K-major tile (2 stages)
-//   warp 8     Q load (TMA) and the MMA issuer (one thread)
-//   warp 9     TMEM allocator
-// The MMA thread issues QK(j) before PV(j-1) so the softmax of tile j
-// overlaps PV(j-1) on the tensor pipe.  The running max is updated lazily
-// (only when a tile's max exceeds it by more than 2^8 in the exp2 domain), so
-// the O rescale in TMEM is rare.
+// TMEM (512 columns): O half [0, 256), two score buffers S [256, 320) for
+// tiles of 32 selected rows, and Q[:, 0:384] as the A operand of Q K^T
+// [320, 512) (two bf16 per column).  Q[:, 384:576] stays in shared memory, so
+// Q K^T runs 24 k-steps with A in TMEM and 12 with A in shared memory.  The
+// softmax writes P (bf16) over the first 16 columns of its score buffer, and
+// P V takes A = P from TMEM and B = V straight from the gathered tile
+// (MN-major).
 //
-// Split-KV (decode): a cluster may take a contiguous range of 64-row tiles of
-// a token; it then writes fp32 (O / l, lse) partials merged by combine_kernel.
+// One thread issues at most about one tcgen05.mma per ~50 cycles, far less
+// than the tensor core retires at N = 32, so three warps issue MMAs, each
+// into its own accumulator: Q K^T of the even tiles, Q K^T of the odd tiles,
+// and P V of every tile (O has a single issuer, so its updates stay ordered).
+//
+// Warp roles (480 threads):
+//   warps 0-3   softmax and epilogue; thread h = head h = TMEM lane h.  They
+//               also copy Q[:, 0:384] into TMEM at the start.
+//   warps 4-11  gather: 16-byte cp.async of the selected rows (full 1152 B)
+//               into a 128-byte-swizzled K-major tile, 4-stage ring
+//   warp 12     TMEM allocation; lane 0 loads Q[:, 384:576] with TMA and
+//               issues Q K^T of the even tiles
+//   warp 13     lane 0 issues Q K^T of the odd tiles
+//   warp 14     lane 0 issues P V
+// The running max is updated lazily (only when a tile's max exceeds it by
+// more than 2^8 in the exp2 domain), so the O rescale in TMEM is rare.
+//
+// Split-KV (decode): a CTA may take a contiguous range of tiles of a token; it
+// then writes fp32 (O / l, lse) partials merged by combine_kernel.
 #pragma once
 
 #include <cstdint>
@@ -46,30 +54,37 @@ namespace mla_tc {
 constexpr int kHeads = 128;
 constexpr int kDqk = 576;
 constexpr int kDv = 512;
-constexpr int kRows = 64;               // selected rows per tile
-constexpr int kLocalBlocks = 5;         // 64-column blocks held per CTA
-constexpr int kKSteps = 18;             // 288 / 16 MMA k-steps per CTA for QK
-constexpr int kQBlockBytes = kHeads * 128;         // 16 KiB
-constexpr int kKVBlockBytes = kRows * 128;         // 8 KiB
-constexpr int kStageBytes = kLocalBlocks * kKVBlockBytes;  // 40 KiB
-constexpr int kStages = 2;
-constexpr int kPBytes = kHeads * kRows * 2;        // 16 KiB
-constexpr int kXBytes = kHeads * kRows * 4;        // 32 KiB
-constexpr int kThreads = 320;
+constexpr int kHalf = 256;              // output columns per CTA
+constexpr int kRows = 32;               // selected rows per tile (N of Q K^T)
+constexpr int kRowChunks = kDqk / 8;    // 72 chunks of 16 B per latent row
+constexpr int kQTmemD = 384;            // Q columns held in TMEM
+constexpr int kQSmemBlocks = (kDqk - kQTmemD) / 64;  // 3 blocks of 64 columns
+constexpr int kKStepsT = kQTmemD / 16;  // 24 k-steps with A in TMEM
+constexpr int kKSteps = kDqk / 16;      // 36
+constexpr int kStages = 4;
+constexpr int kBlk = kRows * 128;                  // one 64-column block of a tile: 4 KiB
+constexpr int kStageBytes = (kDqk / 64) * kBlk;    // 36 KiB
+constexpr int kQBlk = kHeads * 128;                // 16 KiB
+constexpr int kGatherWarps = 8;
+constexpr int kGatherThreads = 32 * kGatherWarps;
+constexpr int kMmaWarp = 4 + kGatherWarps;   // first of the three issuing warps
+constexpr int kThreads = 32 * (kMmaWarp + 3);
 constexpr int kTmemCols = 512;
-constexpr int kSCol = 256;              // TMEM column of S buffer 0
+constexpr int kTmemS = 256;             // two score buffers of kRows columns
+constexpr int kTmemQ = 320;
 constexpr float kRescaleThreshold = 8.f;
+static_assert(kTmemQ + kQTmemD / 2 == kTmemCols, "TMEM layout");
+static_assert(kGatherThreads == 8 * kRows, "gather: 8 threads per selected row");
 
-constexpr int kOffQ = 0;
-constexpr int kOffKV = kOffQ + kLocalBlocks * kQBlockBytes;
-constexpr int kOffP = kOffKV + kStages * kStageBytes;
-constexpr int kOffX = kOffP + 2 * kPBytes;
-constexpr int kOffBar = kOffX + kXBytes;
-constexpr int kNumBars = 20;
+constexpr int kOffKV = 0;
+constexpr int kOffQ = kOffKV + kStages * kStageBytes;
+constexpr int kOffBar = kOffQ + kQSmemBlocks * kQBlk;
+constexpr int kNumBars = 2 * kStages + 12;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;
 
 struct Params {
+  const __nv_bfloat16* q;    // [total_q, 128, 576]
   const __nv_bfloat16* kv;   // [total_kv, 576]
   const int32_t* idx;        // [rows of this launch, k], relative to row0
   int k;
@@ -78,7 +93,7 @@ struct Params {
   const int32_t* cu_kv;
   int num_seqs;
   int64_t row0;
-  int nsplit;                // clusters per query row
+  int nsplit;                // CTA pairs per query row
   int tiles_per_split;
   __nv_bfloat16* out;        // nsplit == 1: [rows, 128, 512], relative to row0
   float* lse;                // nsplit == 1: [rows, 128] or nullptr
@@ -97,7 +112,15 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+__device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
     mla_kernel(const __grid_constant__ CUtensorMap tm_q, const Params P) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte aligned base, derived by pointer arithmetic on the shared array
@@ -105,25 +128,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar0 = sbase + kOffBar;
-  const uint32_t q_full = bar0;
-  auto kv_full = [&](int s) { return bar0 + 8u * (1 + s); };
-  auto kv_empty = [&](int s) { return bar0 + 8u * (3 + s); };
-  auto s_full = [&](int s) { return bar0 + 8u * (5 + s); };
-  auto s_empty = [&](int s) { return bar0 + 8u * (7 + s); };
-  auto p_full = [&](int s) { return bar0 + 8u * (9 + s); };
-  auto p_empty = [&](int s) { return bar0 + 8u * (11 + s); };
-  const uint32_t o_ready = bar0 + 8u * 13;
-  const uint32_t x_full = bar0 + 8u * 14;
-  const uint32_t x_empty = bar0 + 8u * 15;
-  const uint32_t drain_bar = bar0 + 8u * 16;
+  auto kv_full = [&](int s) { return bar0 + 8u * s; };
+  auto kv_empty = [&](int s) { return bar0 + 8u * (kStages + s); };
+  const uint32_t qt_full = bar0 + 8u * (2 * kStages);      // Q columns in TMEM (128 arrivals)
+  const uint32_t qs_full = bar0 + 8u * (2 * kStages + 1);  // Q columns in smem (TMA)
+  auto s_full = [&](int b) { return bar0 + 8u * (2 * kStages + 2 + b); };   // S of a tile ready
+  auto s_free = [&](int b) { return bar0 + 8u * (2 * kStages + 4 + b); };   // P V of that buffer done
+  auto p_full = [&](int b) { return bar0 + 8u * (2 * kStages + 6 + b); };   // P written
+  const uint32_t o_ready = bar0 + 8u * (2 * kStages + 8);
+  auto drain_bar = [&](int r) { return bar0 + 8u * (2 * kStages + 9 + r); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t rank = cluster_ctarank();
-  const uint32_t peer = rank ^ 1u;
 
-  // the work unit of this cluster
+  // the work unit of this CTA: (query row, split, output half)
+  const int half = static_cast<int>(blockIdx.x & 1u);
   const int64_t unit = blockIdx.x >> 1;
   const int64_t rrel = unit / P.nsplit;
   const int split = static_cast<int>(unit % P.nsplit);
@@ -138,166 +158,165 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int32_t* __restrict__ idx_row = P.idx + rrel * static_cast<int64_t>(P.k);
 
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(kv_full(s), 128);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(kv_full(s), kGatherThreads);
       mbar_init(kv_empty(s), 1);
-      mbar_init(s_full(s), 1);
-      mbar_init(s_empty(s), 128);
-      mbar_init(p_full(s), 128);
-      mbar_init(p_empty(s), 1);
+    }
+    mbar_init(qt_full, 128);
+    mbar_init(qs_full, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(s_full(b), 1);
+      mbar_init(s_free(b), 1);
+      mbar_init(p_full(b), 128);
     }
     mbar_init(o_ready, 1);
-    mbar_init(x_full, 128);
-    mbar_init(x_empty, 128);
-    mbar_init(drain_bar, 1);
+    for (int r = 0; r < 3; ++r) mbar_init(drain_bar(r), 1);
     *abort_flag = 0;
     fence_mbar_init();
     fence_proxy_async_smem();
+    tma_prefetch_desc(&tm_q);
   }
-  if (warp == 9) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+  if (warp == kMmaWarp) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
   tc_fence_before();
   __syncthreads();
-  cluster_sync();  // the peer's barriers exist before any remote access
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp >= 4 && warp < 8) {
+  if (warp >= 4 && warp < kMmaWarp) {
     // ------------------------------------------------------------ gather
-    const int pt = threadIdx.x - 128;
-    bool ok = true;
-    for (int j = 0; j < nt && ok; ++j) {
-      const int st = j & 1;
-      if (j >= 2 && !mbar_wait(kv_empty(st), ((j >> 1) - 1) & 1, abort_flag)) { ok = false; break; }
-      const uint32_t stage = sbase + kOffKV + st * kStageBytes;
-      const int e_base = (t_begin + j) * kRows;
-#pragma unroll 4
-      for (int m = 0; m < (kRows * kLocalBlocks * 8) / 128; ++m) {
-        const int c = pt + 128 * m;
-        const int i = c / (kLocalBlocks * 8);
-        const int cc = c - i * (kLocalBlocks * 8);
-        const int blk = cc >> 3, q = cc & 7;
-        const int e = e_base + i;
-        const int s = e < P.k ? __ldg(idx_row + e) : -1;
-        const bool valid = s >= 0 && s < n;
-        if (cc == 0 && (s < -1 || s >= n)) flag_error(DSA_DEVERR_BAD_INDEX);
-        const __nv_bfloat16* src =
-            P.kv + (valid ? (geo.kv0 + s) * kDqk : 0) + (4 * rank + blk) * 64 + q * 8;
-        const uint32_t dst = stage + blk * kKVBlockBytes + i * 128 + ((q ^ (i & 7)) << 4);
-        cp_async_16(dst, src, valid ? 16u : 0u);
-      }
-      cp_async_commit();
-      cp_async_wait<0>();
-      fence_proxy_async_smem();
-      mbar_arrive(kv_full(st));
+    // Thread gt copies row i = gt / 8 of each tile, 16-byte chunks 8u + gt % 8
+    // (u = 0..8), so each warp instruction covers four full 128-byte segments.
+    // The selected position is loaded two tiles ahead; completion of a
+    // thread's copies is tracked by the stage's mbarrier (no blocking wait).
+    const int gt = threadIdx.x - 128;
+    const int i = gt >> 3, t8 = gt & 7;
+    auto load_idx = [&](int j) -> int {
+      const int e = (t_begin + j) * kRows + i;
+      return (j < nt && e < P.k) ? __ldg(idx_row + e) : -1;
+    };
+    int s_cur = load_idx(0), s_next = load_idx(1);
+    for (int j = 0; j < nt; ++j) {
+      const int s = s_cur;
+      s_cur = s_next;
+      s_next = load_idx(j + 2);
+      const int st = j % kStages;
+      if (j >= kStages && !warp_wait(kv_empty(st), ((j / kStages) - 1) & 1, abort_flag)) break;
+      const bool valid = s >= 0 && s < n;
+      if (t8 == 0 && (s < -1 || s >= n)) flag_error(DSA_DEVERR_BAD_INDEX);
+      const __nv_bfloat16* src = P.kv + (valid ? (geo.kv0 + s) * kDqk : 0) + t8 * 8;
+      const uint32_t dst = sbase + kOffKV + st * kStageBytes + i * 128 + ((t8 ^ (i & 7)) << 4);
+#pragma unroll
+      for (int u = 0; u < kDqk / 64; ++u) cp_async_16(dst + u * kBlk, src + u * 64, valid ? 16u : 0u);
+      cp_async_arrive_noinc(kv_full(st));
     }
-  } else if (warp == 8) {
-    // ------------------------------------------------------------ Q load + MMA
+    // no copy may still be in flight when the CTA exits
+    cp_async_commit();
+    cp_async_wait<0>();
+  } else if (warp >= kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuers
+    const int role = warp - kMmaWarp;   // 0: QK even tiles, 1: QK odd tiles, 2: PV
     if (lane == 0 && nt > 0) {
-      mbar_arrive_expect_tx(q_full, kLocalBlocks * kQBlockBytes);
-      for (int b = 0; b < kLocalBlocks; ++b)
-        tma_load_2d(sbase + kOffQ + b * kQBlockBytes, &tm_q, (4 * rank + b) * 64,
-                    static_cast<int32_t>(row * kHeads), q_full);
-      const uint32_t idesc_qk = make_idesc(1, 1, kHeads, kRows, 0, 0);
-      const uint32_t idesc_pv = make_idesc(1, 1, kHeads, 256, 0, 1);
-      bool ok = mbar_wait(q_full, 0, abort_flag);
-      tc_fence_after();
-      auto issue_pv = [&](int i) -> bool {
-        const int sb = i & 1;
-        if (!mbar_wait(p_full(sb), (i >> 1) & 1, abort_flag)) return false;
-        tc_fence_after();
-        const uint32_t pa = sbase + kOffP + sb * kPBytes;
-        const uint32_t va = sbase + kOffKV + sb * kStageBytes;
-#pragma unroll
-        for (int ks = 0; ks < kRows / 16; ++ks)
-          mma_bf16(tmem, make_desc_sw128(pa + ks * 32, 16, 1024),
-                   make_desc_sw128(va + ks * 2048, kKVBlockBytes, 1024), idesc_pv,
-                   (i > 0 || ks > 0) ? 1u : 0u);
-        mma_commit(p_empty(sb));
-        mma_commit(kv_empty(sb));
-        mma_commit(o_ready);
-        return true;
-      };
-      for (int j = 0; j < nt && ok; ++j) {
-        const int st = j & 1;
-        if (!mbar_wait(kv_full(st), (j >> 1) & 1, abort_flag)) { ok = false; break; }
-        if (j >= 2 && !mbar_wait(s_empty(st), ((j >> 1) - 1) & 1, abort_flag)) { ok = false; break; }
-        tc_fence_after();
-        fence_proxy_async_smem();
-        const uint32_t stage = sbase + kOffKV + st * kStageBytes;
-#pragma unroll
-        for (int g = 0; g < kKSteps; ++g) {
-          const int gk = kKSteps * rank + g;          // global k-step (16 columns)
-          const int lb = (gk >> 2) - 4 * rank;        // local 64-column block
-          const int sub = gk & 3;
-          mma_bf16(tmem + kSCol + st * kRows,
-                   make_desc_sw128(sbase + kOffQ + lb * kQBlockBytes + sub * 32, 16, 1024),
-                   make_desc_sw128(stage + lb * kKVBlockBytes + sub * 32, 16, 1024), idesc_qk,
-                   g > 0 ? 1u : 0u);
-        }
-        mma_commit(s_full(st));
-        if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
+      if (role == 0) {
+        mbar_arrive_expect_tx(qs_full, kQSmemBlocks * kQBlk);
+        for (int b = 0; b < kQSmemBlocks; ++b)
+          tma_load_2d(sbase + kOffQ + b * kQBlk, &tm_q, kQTmemD + b * 64, static_cast<int32_t>(row * kHeads),
+                      qs_full);
       }
-      if (ok && nt > 0) issue_pv(nt - 1);
-      mma_commit(drain_bar);
-      drain_wait(drain_bar, 0);
-      drain_wait(q_full, 0);
+      bool ok = true;
+      if (role < 2) {
+        const uint32_t idesc_qk = make_idesc(1, 1, kHeads, kRows, 0, 0);
+        ok = mbar_wait(qs_full, 0, abort_flag) && mbar_wait(qt_full, 0, abort_flag);
+        const uint32_t sacc = tmem + kTmemS + role * kRows;
+        for (int j = role; j < nt && ok; j += 2) {
+          const int st = j % kStages;
+          if (!mbar_wait(kv_full(st), (j / kStages) & 1, abort_flag)) { ok = false; break; }
+          if (j >= 2 && !mbar_wait(s_free(role), ((j >> 1) - 1) & 1, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          // the tile was written by cp.async (generic proxy); the MMA reads it
+          // through the async proxy
+          fence_proxy_async_smem();
+          const uint32_t stage = sbase + kOffKV + st * kStageBytes;
+#pragma unroll
+          for (int g = 0; g < kKSteps; ++g) {
+            const uint64_t bdesc = make_desc(stage + (g >> 2) * kBlk + (g & 3) * 32, 16, 1024, kSwizzle128B);
+            if (g < kKStepsT) {
+              mma_bf16_ta(sacc, tmem + kTmemQ + 8 * g, bdesc, idesc_qk, g > 0 ? 1u : 0u);
+            } else {
+              const int gs = g - kKStepsT;
+              mma_bf16(sacc, make_desc(sbase + kOffQ + (gs >> 2) * kQBlk + (gs & 3) * 32, 16, 1024, kSwizzle128B),
+                       bdesc, idesc_qk, 1u);
+            }
+          }
+          mma_commit(s_full(role));
+        }
+        drain_wait(qs_full, 0);
+      } else {
+        const uint32_t idesc_pv = make_idesc(1, 1, kHeads, kHalf, 0, 1);
+        for (int j = 0; j < nt; ++j) {
+          const int st = j % kStages, pb = j & 1;
+          if (!mbar_wait(kv_full(st), (j / kStages) & 1, abort_flag)) break;
+          if (!mbar_wait(p_full(pb), (j >> 1) & 1, abort_flag)) break;
+          tc_fence_after();
+          fence_proxy_async_smem();
+          const uint32_t va = sbase + kOffKV + st * kStageBytes + (4 * half) * kBlk;
+#pragma unroll
+          for (int ks = 0; ks < kRows / 16; ++ks)
+            mma_bf16_ta(tmem, tmem + kTmemS + pb * kRows + 8 * ks,
+                        make_desc(va + ks * 2048, kBlk, 1024, kSwizzle128B), idesc_pv, (j > 0 || ks > 0) ? 1u : 0u);
+          mma_commit(s_free(pb));
+          mma_commit(kv_empty(st));
+          mma_commit(o_ready);
+        }
+      }
+      mma_commit(drain_bar(role));
+      drain_wait(drain_bar(role), 0);
     }
-  } else if (warp < 4) {
+  } else {
     // ------------------------------------------------------------ softmax
     const int h = threadIdx.x;
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    const uint32_t x_local = sbase + kOffX;
-    const uint32_t x_peer = mapa_shared(x_local, peer);
-    const uint32_t x_full_peer = mapa_shared(x_full, peer);
-    const uint32_t x_empty_peer = mapa_shared(x_empty, peer);
-    float m_use = -INFINITY, l = 0.f;
     bool ok = true;
-    for (int j = 0; j < nt; ++j) {
-      const int sb = j & 1;
-      const int e0 = (t_begin + j) * kRows + lane;
-      const int s0 = e0 < P.k ? __ldg(idx_row + e0) : -1;
-      const int s1 = e0 + 32 < P.k ? __ldg(idx_row + e0 + 32) : -1;
-      const uint32_t mlo = __ballot_sync(0xffffffffu, s0 >= 0 && s0 < n);
-      const uint32_t mhi = __ballot_sync(0xffffffffu, s1 >= 0 && s1 < n);
-
-      if (!warp_wait(s_full(sb), (j >> 1) & 1, abort_flag)) { ok = false; break; }
-      tc_fence_after();
-      uint32_t a[32], bq[32];
-      tmem_ld32(t_lane + kSCol + sb * kRows, a);
-      tmem_ld32(t_lane + kSCol + sb * kRows + 32, bq);
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(s_empty(sb));
-
-      // swap partial scores with the peer CTA
-      if (j >= 1 && !warp_wait<true>(x_empty, (j - 1) & 1, abort_flag)) { ok = false; break; }
+    if (nt > 0) {
+      // Q[:, 0:384] of head h into TMEM columns [320, 512), two bf16 per column
+      const __nv_bfloat16* qh = P.q + (row * kHeads + h) * kDqk;
+#pragma unroll 1
+      for (int c = 0; c < kQTmemD / 64; ++c) {
+        uint32_t r[32];
 #pragma unroll
-      for (int c4 = 0; c4 < 16; ++c4) {
-        const uint32_t* src = c4 < 8 ? &a[4 * c4] : &bq[4 * (c4 - 8)];
-        st_cluster_v4(x_peer + h * 256 + ((c4 ^ (h & 15)) << 4), __uint_as_float(src[0]),
-                      __uint_as_float(src[1]), __uint_as_float(src[2]), __uint_as_float(src[3]));
+        for (int v = 0; v < 8; ++v) {
+          const uint4 x = ldg_nc_v4(qh + c * 64 + v * 8);
+          r[4 * v] = x.x; r[4 * v + 1] = x.y; r[4 * v + 2] = x.z; r[4 * v + 3] = x.w;
+        }
+        tmem_st32(t_lane + kTmemQ + 32 * c, r);
       }
-      mbar_arrive_cluster(x_full_peer);
-      if (!warp_wait<true>(x_full, j & 1, abort_flag)) { ok = false; break; }
-      float z[64];
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(qt_full);
+    }
+    float m_use = -INFINITY, l = 0.f;
+    auto load_sel = [&](int j) -> int {
+      const int e = (t_begin + j) * kRows + lane;
+      return (j < nt && e < P.k) ? __ldg(idx_row + e) : -1;
+    };
+    int sel_next = load_sel(0);
+    for (int j = 0; j < nt; ++j) {
+      const int pb = j & 1;
+      const int sel = sel_next;
+      sel_next = load_sel(j + 1);
+      const uint32_t mask = __ballot_sync(0xffffffffu, sel >= 0 && sel < n);
+      if (!warp_wait(s_full(pb), (j >> 1) & 1, abort_flag)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t a[32];
+      tmem_ld32(t_lane + kTmemS + pb * kRows, a);
+      tmem_wait_ld();
+
+      float z[kRows];
       float mt = -INFINITY;
 #pragma unroll
-      for (int c4 = 0; c4 < 16; ++c4) {
-        const float4 pv = *reinterpret_cast<const float4*>(smem + kOffX + h * 256 + ((c4 ^ (h & 15)) << 4));
-        const uint32_t* own = c4 < 8 ? &a[4 * c4] : &bq[4 * (c4 - 8)];
-        const float pvv[4] = {pv.x, pv.y, pv.z, pv.w};
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int i = 4 * c4 + u;
-          const bool valid = ((i < 32 ? (mlo >> i) : (mhi >> (i - 32))) & 1u) != 0u;
-          const float sval = __uint_as_float(own[u]) + pvv[u];
-          z[i] = valid ? sval * P.c_log2 : -INFINITY;
-          mt = fmaxf(mt, z[i]);
-        }
+      for (int i = 0; i < kRows; ++i) {
+        z[i] = ((mask >> i) & 1u) ? __uint_as_float(a[i]) * P.c_log2 : -INFINITY;
+        mt = fmaxf(mt, z[i]);
       }
-      mbar_arrive_cluster(x_empty_peer);
-
       float alpha = 1.f;
       bool resc = false;
       if (mt > m_use + kRescaleThreshold) {
@@ -305,10 +324,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         m_use = mt;
       }
       l *= alpha;
-      uint32_t pk[32];
+      uint32_t pk[kRows / 2];
       float lsum = 0.f;
 #pragma unroll
-      for (int i = 0; i < 64; i += 2) {
+      for (int i = 0; i < kRows; i += 2) {
         const float p0 = m_use == -INFINITY ? 0.f : ex2(z[i] - m_use);
         const float p1 = m_use == -INFINITY ? 0.f : ex2(z[i + 1] - m_use);
         pk[i >> 1] = pack_bf16(p0, p1);
@@ -317,19 +336,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       l += lsum;
 
-      if (j >= 2 && !warp_wait(p_empty(sb), ((j >> 1) - 1) & 1, abort_flag)) { ok = false; break; }
-      uint8_t* prow = smem + kOffP + sb * kPBytes + h * 128;
-#pragma unroll
-      for (int cc = 0; cc < 8; ++cc)
-        *reinterpret_cast<uint4*>(prow + ((cc ^ (h & 7)) << 4)) =
-            make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
-      fence_proxy_async_smem();
+      // P over the first 16 columns of this score buffer (rows 2c, 2c+1 in
+      // column c, lower row in the low half), the A operand of P V
+      tmem_st16(t_lane + kTmemS + pb * kRows, pk);
+      tmem_wait_st();
       if (__any_sync(0xffffffffu, resc)) {
         // O must hold PV(j-1) before it is rescaled
         if (!warp_wait(o_ready, (j - 1) & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll 1
-        for (int c = 0; c < 8; ++c) {
+        for (int c = 0; c < kHalf / 32; ++c) {
           uint32_t o[32];
           tmem_ld32(t_lane + 32 * c, o);
           tmem_wait_ld();
@@ -340,7 +356,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tmem_wait_st();
         tc_fence_before();
       }
-      mbar_arrive(p_full(sb));
+      tc_fence_before();
+      mbar_arrive(p_full(pb));
     }
 
     // ---- epilogue: O / l (and lse)
@@ -354,9 +371,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const float inv = l > 0.f ? 1.f / l : 0.f;
     const float lse_v = l > 0.f ? (m_use + __log2f(l)) * 0.6931471805599453f : -INFINITY;
     if (P.nsplit == 1) {
-      __nv_bfloat16* orow = P.out + (rrel * kHeads + h) * kDv + rank * 256;
+      __nv_bfloat16* orow = P.out + (rrel * kHeads + h) * kDv + half * kHalf;
 #pragma unroll 1
-      for (int c = 0; c < 8; ++c) {
+      for (int c = 0; c < kHalf / 32; ++c) {
         uint32_t o[32];
         if (have_o) { tmem_ld32(t_lane + 32 * c, o); tmem_wait_ld(); }
         else {
@@ -373,11 +390,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           *reinterpret_cast<uint4*>(orow + 32 * c + 8 * v) = pk4;
         }
       }
-      if (rank == 0 && P.lse) P.lse[rrel * kHeads + h] = lse_v;
+      if (half == 0 && P.lse) P.lse[rrel * kHeads + h] = lse_v;
     } else {
-      float* orow = P.part_o + (unit * kHeads + h) * kDv + rank * 256;
+      float* orow = P.part_o + (unit * kHeads + h) * kDv + half * kHalf;
 #pragma unroll 1
-      for (int c = 0; c < 8; ++c) {
+      for (int c = 0; c < kHalf / 32; ++c) {
         uint32_t o[32];
         if (have_o) { tmem_ld32(t_lane + 32 * c, o); tmem_wait_ld(); }
         else {
@@ -390,14 +407,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               make_float4(__uint_as_float(o[4 * v]) * inv, __uint_as_float(o[4 * v + 1]) * inv,
                           __uint_as_float(o[4 * v + 2]) * inv, __uint_as_float(o[4 * v + 3]) * inv);
       }
-      if (rank == 0) P.part_lse[unit * kHeads + h] = lse_v;
+      if (half == 0) P.part_lse[unit * kHeads + h] = lse_v;
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  cluster_sync();  // no remote access may target an exited CTA
-  if (warp == 9) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
