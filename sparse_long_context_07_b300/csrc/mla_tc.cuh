@@ -16,10 +16,10 @@
 // TMEM (512 columns): O half [0, 256), two score buffers S [256, 320) for
 // tiles of 32 selected rows, and Q[:, 0:384] as the A operand of Q K^T
 // [320, 512) (two bf16 per column).  Q[:, 384:576] stays in shared memory, so
-// Q K^T runs 24 k-steps with A in TMEM and 12 with A in shared memory.  The
-// softmax writes P (bf16) over the first 16 columns of its score buffer, and
-// P V takes A = P from TMEM and B = V straight from the gathered tile
-// (MN-major).
+// Q K^T runs 24 k-steps with A in TMEM and 12 with A in shared memory.  P
+// (bf16) goes to shared memory (64-byte swizzle, two buffers), so a score
+// buffer is free again as soon as the softmax has read it; P V takes A = P and
+// B = V straight from the gathered tile (MN-major).
 //
 // One thread issues at most about one tcgen05.mma per ~50 cycles, far less
 // than the tensor core retires at N = 32, so three warps issue MMAs, each
@@ -63,6 +63,7 @@ constexpr int kKStepsT = kQTmemD / 16;  // 24 k-steps with A in TMEM
 constexpr int kKSteps = kDqk / 16;      // 36
 constexpr int kStages = 4;
 constexpr int kBlk = kRows * 128;                  // one 64-column block of a tile: 4 KiB
+constexpr int kPBytes = kHeads * kRows * 2;        // 8 KiB
 constexpr int kStageBytes = (kDqk / 64) * kBlk;    // 36 KiB
 constexpr int kQBlk = kHeads * 128;                // 16 KiB
 constexpr int kGatherWarps = 8;
@@ -78,8 +79,9 @@ static_assert(kGatherThreads == 8 * kRows, "gather: 8 threads per selected row")
 
 constexpr int kOffKV = 0;
 constexpr int kOffQ = kOffKV + kStages * kStageBytes;
-constexpr int kOffBar = kOffQ + kQSmemBlocks * kQBlk;
-constexpr int kNumBars = 2 * kStages + 12;
+constexpr int kOffP = kOffQ + kQSmemBlocks * kQBlk;
+constexpr int kOffBar = kOffP + 2 * kPBytes;
+constexpr int kNumBars = 2 * kStages + 14;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;
 
@@ -133,10 +135,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t qt_full = bar0 + 8u * (2 * kStages);      // Q columns in TMEM (128 arrivals)
   const uint32_t qs_full = bar0 + 8u * (2 * kStages + 1);  // Q columns in smem (TMA)
   auto s_full = [&](int b) { return bar0 + 8u * (2 * kStages + 2 + b); };   // S of a tile ready
-  auto s_free = [&](int b) { return bar0 + 8u * (2 * kStages + 4 + b); };   // P V of that buffer done
+  auto s_empty = [&](int b) { return bar0 + 8u * (2 * kStages + 4 + b); };  // S read by the softmax
   auto p_full = [&](int b) { return bar0 + 8u * (2 * kStages + 6 + b); };   // P written
-  const uint32_t o_ready = bar0 + 8u * (2 * kStages + 8);
-  auto drain_bar = [&](int r) { return bar0 + 8u * (2 * kStages + 9 + r); };
+  auto p_empty = [&](int b) { return bar0 + 8u * (2 * kStages + 8 + b); };  // P V of that buffer done
+  const uint32_t o_ready = bar0 + 8u * (2 * kStages + 10);
+  auto drain_bar = [&](int r) { return bar0 + 8u * (2 * kStages + 11 + r); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
 
@@ -166,8 +169,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(qs_full, 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(s_full(b), 1);
-      mbar_init(s_free(b), 1);
+      mbar_init(s_empty(b), 128);
       mbar_init(p_full(b), 128);
+      mbar_init(p_empty(b), 1);
     }
     mbar_init(o_ready, 1);
     for (int r = 0; r < 3; ++r) mbar_init(drain_bar(r), 1);
@@ -227,24 +231,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t idesc_qk = make_idesc(1, 1, kHeads, kRows, 0, 0);
         ok = mbar_wait(qs_full, 0, abort_flag) && mbar_wait(qt_full, 0, abort_flag);
         const uint32_t sacc = tmem + kTmemS + role * kRows;
+        // descriptors are formed once; a k-step adds its byte offset >> 4 to
+        // the start-address field (all addresses stay below 2^18, so the
+        // 14-bit field cannot overflow)
+        const uint64_t kv_desc0 = make_desc(sbase + kOffKV, 16, 1024, kSwizzle128B);
+        const uint64_t q_desc0 = make_desc(sbase + kOffQ, 16, 1024, kSwizzle128B);
         for (int j = role; j < nt && ok; j += 2) {
           const int st = j % kStages;
           if (!mbar_wait(kv_full(st), (j / kStages) & 1, abort_flag)) { ok = false; break; }
-          if (j >= 2 && !mbar_wait(s_free(role), ((j >> 1) - 1) & 1, abort_flag)) { ok = false; break; }
+          if (j >= 2 && !mbar_wait(s_empty(role), ((j >> 1) - 1) & 1, abort_flag)) { ok = false; break; }
           tc_fence_after();
           // the tile was written by cp.async (generic proxy); the MMA reads it
           // through the async proxy
           fence_proxy_async_smem();
-          const uint32_t stage = sbase + kOffKV + st * kStageBytes;
+          const uint64_t bdesc0 = kv_desc0 + static_cast<uint64_t>((st * kStageBytes) >> 4);
 #pragma unroll
           for (int g = 0; g < kKSteps; ++g) {
-            const uint64_t bdesc = make_desc(stage + (g >> 2) * kBlk + (g & 3) * 32, 16, 1024, kSwizzle128B);
+            const uint64_t bdesc = bdesc0 + static_cast<uint64_t>(((g >> 2) * kBlk + (g & 3) * 32) >> 4);
             if (g < kKStepsT) {
               mma_bf16_ta(sacc, tmem + kTmemQ + 8 * g, bdesc, idesc_qk, g > 0 ? 1u : 0u);
             } else {
               const int gs = g - kKStepsT;
-              mma_bf16(sacc, make_desc(sbase + kOffQ + (gs >> 2) * kQBlk + (gs & 3) * 32, 16, 1024, kSwizzle128B),
-                       bdesc, idesc_qk, 1u);
+              mma_bf16(sacc, q_desc0 + static_cast<uint64_t>(((gs >> 2) * kQBlk + (gs & 3) * 32) >> 4), bdesc,
+                       idesc_qk, 1u);
             }
           }
           mma_commit(s_full(role));
@@ -259,11 +268,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           fence_proxy_async_smem();
           const uint32_t va = sbase + kOffKV + st * kStageBytes + (4 * half) * kBlk;
+          const uint32_t pa = sbase + kOffP + pb * kPBytes;
 #pragma unroll
           for (int ks = 0; ks < kRows / 16; ++ks)
-            mma_bf16_ta(tmem, tmem + kTmemS + pb * kRows + 8 * ks,
-                        make_desc(va + ks * 2048, kBlk, 1024, kSwizzle128B), idesc_pv, (j > 0 || ks > 0) ? 1u : 0u);
-          mma_commit(s_free(pb));
+            mma_bf16(tmem, make_desc(pa + ks * 32, 16, 512, kSwizzle64B),
+                     make_desc(va + ks * 2048, kBlk, 1024, kSwizzle128B), idesc_pv, (j > 0 || ks > 0) ? 1u : 0u);
+          mma_commit(p_empty(pb));
           mma_commit(kv_empty(st));
           mma_commit(o_ready);
         }
@@ -279,15 +289,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (nt > 0) {
       // Q[:, 0:384] of head h into TMEM columns [320, 512), two bf16 per column
       const __nv_bfloat16* qh = P.q + (row * kHeads + h) * kDqk;
+      // 128 columns of Q (256 bytes) per round: 16 loads in flight
 #pragma unroll 1
-      for (int c = 0; c < kQTmemD / 64; ++c) {
-        uint32_t r[32];
+      for (int c = 0; c < kQTmemD / 128; ++c) {
+        uint32_t r0[32], r1[32];
 #pragma unroll
         for (int v = 0; v < 8; ++v) {
-          const uint4 x = ldg_nc_v4(qh + c * 64 + v * 8);
-          r[4 * v] = x.x; r[4 * v + 1] = x.y; r[4 * v + 2] = x.z; r[4 * v + 3] = x.w;
+          const uint4 x = ldg_nc_v4(qh + c * 128 + v * 8);
+          const uint4 y = ldg_nc_v4(qh + c * 128 + 64 + v * 8);
+          r0[4 * v] = x.x; r0[4 * v + 1] = x.y; r0[4 * v + 2] = x.z; r0[4 * v + 3] = x.w;
+          r1[4 * v] = y.x; r1[4 * v + 1] = y.y; r1[4 * v + 2] = y.z; r1[4 * v + 3] = y.w;
         }
-        tmem_st32(t_lane + kTmemQ + 32 * c, r);
+        tmem_st32(t_lane + kTmemQ + 64 * c, r0);
+        tmem_st32(t_lane + kTmemQ + 64 * c + 32, r1);
       }
       tmem_wait_st();
       tc_fence_before();
@@ -309,6 +323,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t a[32];
       tmem_ld32(t_lane + kTmemS + pb * kRows, a);
       tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(s_empty(pb));
 
       float z[kRows];
       float mt = -INFINITY;
@@ -336,10 +352,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       l += lsum;
 
-      // P over the first 16 columns of this score buffer (rows 2c, 2c+1 in
-      // column c, lower row in the low half), the A operand of P V
-      tmem_st16(t_lane + kTmemS + pb * kRows, pk);
-      tmem_wait_st();
+      if (j >= 2 && !warp_wait(p_empty(pb), ((j >> 1) - 1) & 1, abort_flag)) { ok = false; break; }
+      // P row h: 64 bytes, 64-byte swizzle (16-byte chunk c at c ^ ((h >> 1) & 3))
+      uint8_t* prow = smem + kOffP + pb * kPBytes + h * 64;
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc)
+        *reinterpret_cast<uint4*>(prow + ((cc ^ ((h >> 1) & 3)) << 4)) =
+            make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+      fence_proxy_async_smem();
       if (__any_sync(0xffffffffu, resc)) {
         // O must hold PV(j-1) before it is rescaled
         if (!warp_wait(o_ready, (j - 1) & 1, abort_flag)) { ok = false; break; }
