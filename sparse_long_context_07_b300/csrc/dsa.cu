@@ -93,7 +93,9 @@ dsa_status_t device_info(DeviceInfo** out) {
     if (cudaFuncSetAttribute(dsa::idx_tc::indexer_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              dsa::idx_tc::kSmemBytes) != cudaSuccess ||
         cudaFuncSetAttribute(dsa::mla_tc::mla_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             dsa::mla_tc::kSmemBytes) != cudaSuccess)
+                             dsa::mla_tc::kSmemBytes) != cudaSuccess ||
+        cudaFuncSetAttribute(dsa::topk::topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             dsa::topk::kSmemBytes) != cudaSuccess)
       return fail(DSA_ERROR_LAUNCH, "cudaFuncSetAttribute failed: %s",
                   cudaGetErrorString(cudaGetLastError()));
     d.attrs_set = true;
@@ -279,7 +281,7 @@ dsa_status_t launch_topk(const dsa_batch_t* b, const float* scores, int64_t ld, 
                          float* vals, int64_t r0, int64_t r1, cudaStream_t s, Tracer& tr) {
   for (int64_t c = r0; c < r1; c += 2147483647ll) {
     const int64_t e = std::min<int64_t>(r1, c + 2147483647ll);
-    dsa::topk::topk_kernel<<<static_cast<unsigned>(e - c), dsa::topk::kThreads, 0, s>>>(
+    dsa::topk::topk_kernel<<<static_cast<unsigned>(e - c), dsa::topk::kThreads, dsa::topk::kSmemBytes, s>>>(
         scores + (c - r0) * ld, ld, k, idx + (c - r0) * k, vals ? vals + (c - r0) * k : nullptr,
         b->cu_seqlens_q, b->cu_seqlens_kv, b->num_seqs, c);
     DSA_TRY(check_launch("topk"));

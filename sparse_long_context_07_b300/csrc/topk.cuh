@@ -5,10 +5,20 @@
 // the System Modules of "DeepSeek-V3.2: Pushing the Frontier of Open Large
 // Language Models").  Ties go to the lower position; -0.0 == +0.0.
 //
-// One CTA per row.  Scores map to order-preserving 32-bit keys; three radix
-// passes (11 + 11 + 10 bits, shared-memory histograms) find the exact k-th key
-// T and how many keys equal to T are taken (the lowest positions).  A final
-// ordered pass compacts the selection in ascending position with block scans.
+// One CTA per row.  Scores map to order-preserving 32-bit keys.
+//   pass 1 (row read once): histogram of the top 11 key bits; the bin b* that
+//            holds the k-th largest key and the count above it follow from a
+//            block scan.
+//   pass 2 (row read again): keys in bins above b* are selected outright (one
+//            bit each in a shared-memory bitmap of positions); keys in b* are
+//            kept as candidates (low 21 bits, position) in shared memory.
+//   The candidates are narrowed by two more radix passes in shared memory to
+//   the exact k-th key; the larger ones join the bitmap, the equal ones go to
+//   a tie bitmap of which the lowest positions are taken.  Scanning the
+//   bitmaps in position order writes the selection in ascending order.
+// Rows longer than the bitmaps or whose boundary bin overflows the candidate
+// store (heavy ties) take the general path: three radix passes over the row
+// for the exact k-th key, then an ordered compaction with block scans.
 // Rows with n <= k take every candidate.
 #pragma once
 
@@ -22,6 +32,21 @@ namespace topk {
 constexpr int kThreads = 512;
 constexpr int kBins = 2048;     // histogram bins (11-bit digits)
 constexpr int kPerThread = 8;   // elements per thread per compaction chunk
+constexpr int kMaxFastN = 131072;                 // positions covered by the bitmaps
+constexpr int kBitmapWords = kMaxFastN / 32;
+constexpr int kWordsPerThread = kBitmapWords / kThreads;
+constexpr int kCandCap = 4096;                    // boundary-bin candidates held in smem
+
+struct Smem {
+  uint32_t hist[kBins];
+  uint32_t sel[kBitmapWords];    // selected positions
+  uint32_t tie[kBitmapWords];    // positions whose key equals the k-th key
+  uint32_t cand_key[kCandCap];   // low 21 key bits of the boundary-bin keys
+  int32_t cand_idx[kCandCap];
+  uint32_t warp_sums[32];
+  uint32_t s_digit, s_above, ncand;
+};
+constexpr int kSmemBytes = static_cast<int>(sizeof(Smem));
 
 // Monotone map float -> uint32 (larger float, larger key); -0 maps like +0.
 __device__ __forceinline__ uint32_t order_key(float x) {
@@ -30,32 +55,35 @@ __device__ __forceinline__ uint32_t order_key(float x) {
   return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
-__global__ void __launch_bounds__(kThreads) topk_kernel(
-    const float* __restrict__ scores, int64_t ld, int k, int32_t* __restrict__ idx,
-    float* __restrict__ vals, const int32_t* __restrict__ cu_q, const int32_t* __restrict__ cu_kv,
-    int num_seqs, int64_t row0) {
-  __shared__ uint32_t hist[kBins];
-  __shared__ uint32_t warp_sums[32];
-  __shared__ uint32_t s_digit, s_above;
-
+// The digit (bin index) holding the kr-th largest key of `hist` (nbins bins,
+// thread t owns bins [4t, 4t+4)), and the number of keys in higher bins.
+__device__ __forceinline__ void find_digit(const uint32_t* hist, int nbins, uint32_t kr, Smem& sm) {
   const int tid = threadIdx.x;
-  const int64_t r = row0 + blockIdx.x;
-  const RowGeom g = row_geom(cu_q, cu_kv, num_seqs, r);
-  const int n = g.p + 1;
-  // scores, idx and vals hold the rows of this launch, starting at row0
-  const float* __restrict__ row = scores + (r - row0) * ld;
-  int32_t* __restrict__ out_idx = idx + (r - row0) * static_cast<int64_t>(k);
-  float* __restrict__ out_val = vals ? vals + (r - row0) * static_cast<int64_t>(k) : nullptr;
-
-  if (n <= k) {  // every candidate is selected (uniform per block)
-    for (int i = tid; i < k; i += kThreads) {
-      out_idx[i] = i < n ? i : -1;
-      if (out_val) out_val[i] = i < n ? row[i] : -__int_as_float(0x7f800000);
-    }
-    return;
+  uint32_t c[4], s = 0;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    c[q] = (4 * tid + q < nbins) ? hist[4 * tid + q] : 0u;
+    s += c[q];
   }
+  uint32_t total;
+  const uint32_t incl = block_inclusive_scan<kThreads>(s, sm.warp_sums, total);
+  const uint32_t above = total - incl;  // keys in higher bins than mine
+  if (above < kr && above + s >= kr) {
+    uint32_t a = above;
+#pragma unroll
+    for (int q = 3; q >= 0; --q) {
+      if (a + c[q] >= kr) { sm.s_digit = 4 * tid + q; sm.s_above = a; break; }
+      a += c[q];
+    }
+  }
+  __syncthreads();
+}
 
-  // ---- radix select of the exact k-th largest key
+// General path: exact k-th key by three radix passes over the row, then an
+// ordered compaction with block scans.
+__device__ void select_general(const float* __restrict__ row, int n, int k, int32_t* __restrict__ out_idx,
+                               float* __restrict__ out_val, Smem& sm) {
+  const int tid = threadIdx.x;
   uint32_t prefix = 0, pmask = 0, kr = static_cast<uint32_t>(k);
   const int n4 = n >> 2;
   const float4* __restrict__ row4 = reinterpret_cast<const float4*>(row);
@@ -63,11 +91,11 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(
   for (int pass = 0; pass < 3; ++pass) {
     const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
     const uint32_t dmask = pass == 2 ? 0x3FFu : 0x7FFu;
-    for (int i = tid; i < kBins; i += kThreads) hist[i] = 0;
+    for (int i = tid; i < kBins; i += kThreads) sm.hist[i] = 0;
     __syncthreads();
     auto add = [&](float x) {
       const uint32_t key = order_key(x);
-      if ((key & pmask) == prefix) atomicAdd(&hist[(key >> shift) & dmask], 1u);
+      if ((key & pmask) == prefix) atomicAdd(&sm.hist[(key >> shift) & dmask], 1u);
     };
     for (int i = tid; i < n4; i += kThreads) {
       const float4 v = __ldg(row4 + i);
@@ -75,30 +103,15 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(
     }
     for (int i = 4 * n4 + tid; i < n; i += kThreads) add(__ldg(row + i));
     __syncthreads();
-    // thread t owns bins [4t, 4t+4); find the digit holding the kr-th largest
-    uint32_t c[4], s = 0;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) { c[q] = hist[4 * tid + q]; s += c[q]; }
-    uint32_t total;
-    const uint32_t incl = block_inclusive_scan<kThreads>(s, warp_sums, total);
-    const uint32_t above = total - incl;  // keys in higher bins than mine
-    if (above < kr && above + s >= kr) {
-      uint32_t a = above;
-#pragma unroll
-      for (int q = 3; q >= 0; --q) {
-        if (a + c[q] >= kr) { s_digit = 4 * tid + q; s_above = a; break; }
-        a += c[q];
-      }
-    }
-    __syncthreads();
-    kr -= s_above;
-    prefix |= s_digit << shift;
+    find_digit(sm.hist, kBins, kr, sm);
+    kr -= sm.s_above;
+    prefix |= sm.s_digit << shift;
     pmask |= dmask << shift;
     __syncthreads();
   }
   const uint32_t T = prefix;  // exact k-th largest key; take kr of the keys == T
 
-  // ---- ordered compaction: key > T, or key == T among the first kr such
+  // ordered compaction: key > T, or key == T among the first kr such
   uint32_t base_sel = 0, base_eq = 0;
 #pragma unroll 1
   for (int chunk = 0; chunk < n; chunk += kThreads * kPerThread) {
@@ -125,7 +138,7 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(
     }
     const uint32_t ne = __popc(eq_bits);
     uint32_t tot_eq;
-    const uint32_t excl_eq = block_inclusive_scan<kThreads>(ne, warp_sums, tot_eq) - ne;
+    const uint32_t excl_eq = block_inclusive_scan<kThreads>(ne, sm.warp_sums, tot_eq) - ne;
     uint32_t rank = base_eq + excl_eq, sel_bits = gt_bits;
 #pragma unroll
     for (int q = 0; q < kPerThread; ++q) {
@@ -136,7 +149,7 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(
     }
     const uint32_t ns = __popc(sel_bits);
     uint32_t tot_sel;
-    uint32_t pos = base_sel + block_inclusive_scan<kThreads>(ns, warp_sums, tot_sel) - ns;
+    uint32_t pos = base_sel + block_inclusive_scan<kThreads>(ns, sm.warp_sums, tot_sel) - ns;
 #pragma unroll
     for (int q = 0; q < kPerThread; ++q) {
       if (((sel_bits >> q) & 1u) && pos < static_cast<uint32_t>(k)) {
@@ -148,6 +161,145 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(
     base_sel += tot_sel;
     base_eq += tot_eq;
     if (base_sel >= static_cast<uint32_t>(k)) break;
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) topk_kernel(
+    const float* __restrict__ scores, int64_t ld, int k, int32_t* __restrict__ idx,
+    float* __restrict__ vals, const int32_t* __restrict__ cu_q, const int32_t* __restrict__ cu_kv,
+    int num_seqs, int64_t row0) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
+
+  const int tid = threadIdx.x;
+  const int64_t r = row0 + blockIdx.x;
+  const RowGeom g = row_geom(cu_q, cu_kv, num_seqs, r);
+  const int n = g.p + 1;
+  // scores, idx and vals hold the rows of this launch, starting at row0
+  const float* __restrict__ row = scores + (r - row0) * ld;
+  int32_t* __restrict__ out_idx = idx + (r - row0) * static_cast<int64_t>(k);
+  float* __restrict__ out_val = vals ? vals + (r - row0) * static_cast<int64_t>(k) : nullptr;
+
+  if (n <= k) {  // every candidate is selected (uniform per block)
+    for (int i = tid; i < k; i += kThreads) {
+      out_idx[i] = i < n ? i : -1;
+      if (out_val) out_val[i] = i < n ? row[i] : -__int_as_float(0x7f800000);
+    }
+    return;
+  }
+
+  // ---- pass 1: histogram of the top 11 key bits
+  for (int i = tid; i < kBins; i += kThreads) sm.hist[i] = 0;
+  __syncthreads();
+  const int n4 = n >> 2;
+  const float4* __restrict__ row4 = reinterpret_cast<const float4*>(row);
+  for (int i = tid; i < n4; i += kThreads) {
+    const float4 v = __ldg(row4 + i);
+    atomicAdd(&sm.hist[order_key(v.x) >> 21], 1u);
+    atomicAdd(&sm.hist[order_key(v.y) >> 21], 1u);
+    atomicAdd(&sm.hist[order_key(v.z) >> 21], 1u);
+    atomicAdd(&sm.hist[order_key(v.w) >> 21], 1u);
+  }
+  for (int i = 4 * n4 + tid; i < n; i += kThreads) atomicAdd(&sm.hist[order_key(__ldg(row + i)) >> 21], 1u);
+  __syncthreads();
+  find_digit(sm.hist, kBins, static_cast<uint32_t>(k), sm);
+  const uint32_t bstar = sm.s_digit;
+  const uint32_t kr = static_cast<uint32_t>(k) - sm.s_above;   // keys to take from bin b*
+  const uint32_t cstar = sm.hist[bstar];
+  if (n > kMaxFastN || cstar > static_cast<uint32_t>(kCandCap)) {   // uniform per block
+    __syncthreads();
+    select_general(row, n, k, out_idx, out_val, sm);
+    return;
+  }
+
+  // ---- pass 2: bins above b* are selected, bin b* keeps candidates
+  for (int i = tid; i < kBitmapWords; i += kThreads) { sm.sel[i] = 0u; sm.tie[i] = 0u; }
+  if (tid == 0) sm.ncand = 0u;
+  __syncthreads();
+  auto classify = [&](float x, int i) {
+    const uint32_t key = order_key(x);
+    const uint32_t d = key >> 21;
+    if (d > bstar) {
+      atomicOr(&sm.sel[i >> 5], 1u << (i & 31));
+    } else if (d == bstar) {
+      const uint32_t slot = atomicAdd(&sm.ncand, 1u);
+      sm.cand_key[slot] = key & 0x1FFFFFu;
+      sm.cand_idx[slot] = i;
+    }
+  };
+  for (int i = tid; i < n4; i += kThreads) {
+    const float4 v = __ldg(row4 + i);
+    classify(v.x, 4 * i); classify(v.y, 4 * i + 1); classify(v.z, 4 * i + 2); classify(v.w, 4 * i + 3);
+  }
+  for (int i = 4 * n4 + tid; i < n; i += kThreads) classify(__ldg(row + i), i);
+  __syncthreads();
+
+  // ---- the kr-th largest low-21-bit value among the candidates (two radix
+  // passes in shared memory: bits 20..10, then 9..0)
+  uint32_t prefix = 0, pmask = 0, krr = kr;
+#pragma unroll 1
+  for (int pass = 0; pass < 2; ++pass) {
+    const int shift = pass == 0 ? 10 : 0;
+    const uint32_t dmask = pass == 0 ? 0x7FFu : 0x3FFu;
+    for (int i = tid; i < kBins; i += kThreads) sm.hist[i] = 0;
+    __syncthreads();
+    for (uint32_t c = tid; c < cstar; c += kThreads) {
+      const uint32_t lk = sm.cand_key[c];
+      if ((lk & pmask) == prefix) atomicAdd(&sm.hist[(lk >> shift) & dmask], 1u);
+    }
+    __syncthreads();
+    find_digit(sm.hist, pass == 0 ? kBins : 1024, krr, sm);
+    krr -= sm.s_above;
+    prefix |= sm.s_digit << shift;
+    pmask |= dmask << shift;
+    __syncthreads();
+  }
+  const uint32_t T21 = prefix;   // candidates above it are selected; take krr of the equal ones
+  for (uint32_t c = tid; c < cstar; c += kThreads) {
+    const uint32_t lk = sm.cand_key[c];
+    const int i = sm.cand_idx[c];
+    if (lk > T21) atomicOr(&sm.sel[i >> 5], 1u << (i & 31));
+    else if (lk == T21) atomicOr(&sm.tie[i >> 5], 1u << (i & 31));
+  }
+  __syncthreads();
+
+  // ---- ordered emission: thread t scans bitmap words [8t, 8t+8)
+  const int nwords = (n + 31) >> 5;
+  const int w0 = tid * kWordsPerThread;
+  uint32_t sel_cnt = 0, tie_cnt = 0;
+#pragma unroll
+  for (int q = 0; q < kWordsPerThread; ++q) {
+    if (w0 + q < nwords) {
+      sel_cnt += __popc(sm.sel[w0 + q]);
+      tie_cnt += __popc(sm.tie[w0 + q]);
+    }
+  }
+  uint32_t tot;
+  const uint32_t tie_before = block_inclusive_scan<kThreads>(tie_cnt, sm.warp_sums, tot) - tie_cnt;
+  uint32_t take = tie_before >= krr ? 0u : min(krr - tie_before, tie_cnt);
+  const uint32_t out_cnt = sel_cnt + take;
+  uint32_t pos = block_inclusive_scan<kThreads>(out_cnt, sm.warp_sums, tot) - out_cnt;
+#pragma unroll 1
+  for (int q = 0; q < kWordsPerThread; ++q) {
+    const int w = w0 + q;
+    if (w >= nwords) break;
+    uint32_t bits = sm.sel[w];
+    uint32_t tb = sm.tie[w];
+    while (take > 0u && tb != 0u) {   // the lowest positions of the ties
+      bits |= tb & (0u - tb);
+      tb &= tb - 1u;
+      --take;
+    }
+    while (bits != 0u) {
+      const int b = __ffs(bits) - 1;
+      bits &= bits - 1u;
+      const int i = 32 * w + b;
+      if (pos < static_cast<uint32_t>(k)) {
+        out_idx[pos] = i;
+        if (out_val) out_val[pos] = __ldg(row + i);
+      }
+      ++pos;
+    }
   }
 }
 

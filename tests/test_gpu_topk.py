@@ -80,3 +80,18 @@ def test_topk_all_equal_and_large_k():
     scores = _scores(4, ld, "const", seed=0)
     _check(batch, scores, ld, 16384, range(4), dict(enumerate(lens)))
     _check(batch, _scores(4, ld, "normal", seed=3), ld, 16384, range(4), dict(enumerate(lens)))
+
+
+def test_topk_rows_beyond_the_bitmap_and_boundary_overflow():
+    # rows longer than 131072 candidates take the general path; so does a row
+    # whose boundary histogram bin holds more than 4096 keys (many equal keys
+    # at the k-th value: normal scores with a block of 6000 copies of one value)
+    lens = [140000, 131073, 131072, 9000]
+    k = 2048
+    ld = 140000
+    batch = dsa.Batch(_cu([1] * len(lens)), _cu(lens), [1] * len(lens), lens)
+    scores = _scores(len(lens), ld, "normal", seed=8)
+    row = scores[3]
+    kth = torch.sort(row[:9000], descending=True).values[k - 100]
+    row[1000:7000] = kth
+    _check(batch, scores, ld, k, range(len(lens)), dict(enumerate(lens)))
