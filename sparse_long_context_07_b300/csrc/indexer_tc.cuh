@@ -19,7 +19,7 @@
 //   warp 0      TMA producer: q block of the item, then a ring of key tiles
 //   warp 1      MMA issuer (one thread): 4 x tcgen05.mma kind::f8f6f4 per tile
 //   warp 2      TMEM allocator
-//   warps 4-11  two epilogue warpgroups; warpgroup e handles tokens 2e, 2e+1
+//   warps 4-19  four epilogue warpgroups; warpgroup e handles token e
 // Two TMEM accumulators (2 x 256 columns) let the epilogue of tile i overlap
 // the MMA of tile i+1.
 //
@@ -41,7 +41,8 @@ constexpr int kDim = 128;           // d_I (MMA K), one e4m3 byte each
 constexpr int kHeads = 64;          // H_I
 constexpr int kMaxTokens = 4;       // tokens per item (N = 64 G <= 256)
 constexpr int kStages = 6;          // key-tile ring depth
-constexpr int kThreads = 384;
+constexpr int kEpiGroups = 4;      // epilogue warpgroups, one token each
+constexpr int kThreads = 128 + 128 * kEpiGroups;
 constexpr int kTileBytes = kKeys * kDim;                 // 16 KiB
 constexpr int kQTokenBytes = kHeads * kDim;              // 8 KiB
 constexpr int kQBytes = kMaxTokens * kQTokenBytes;       // 32 KiB
@@ -53,7 +54,7 @@ constexpr int kOffK = 0;
 constexpr int kOffQ = kOffK + kStages * kTileBytes;
 constexpr int kOffW = kOffQ + 2 * kQBytes;
 constexpr int kOffBar = kOffW + 2 * kMaxTokens * kHeads * 4;
-constexpr int kNumBars = 2 * kStages + 2 + 2 + 2 + 2 + 1 + 4;
+constexpr int kNumBars = 2 * kStages + 2 + 2 + 2 + 2 + 1 + 2 * kEpiGroups;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
 
@@ -126,35 +127,24 @@ struct Walker {
   }
 };
 
-__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
-  uint64_t ra, rb, rc, rd;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(ra) : "f"(a.x), "f"(a.y));
-  asm("mov.b64 %0, {%1, %2};" : "=l"(rb) : "f"(b.x), "f"(b.y));
-  asm("mov.b64 %0, {%1, %2};" : "=l"(rc) : "f"(c.x), "f"(c.y));
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(rd) : "l"(ra), "l"(rb), "l"(rc));
-  float2 d;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(rd));
-  return d;
-}
-
 // acc += sum_j w[j] ReLU(x[j]) over 32 heads.  Even heads take ReLU as
 // max(x, 0) (ALU pipe), odd heads as x + |x| = 2 ReLU(x) (FMA pipe) against
 // weights staged at half value; both products then share one packed fp32x2
 // FMA.  Both forms are exact, so the sum equals the plain formula up to the
-// order of the additions.
-__device__ __forceinline__ void reduce_chunk(const uint32_t (&x)[32], const float* w, float2& acc) {
+// order of the additions.  Four independent partial sums keep the FMA chains
+// short.
+__device__ __forceinline__ void reduce_chunk(const uint32_t (&x)[32], const float* w, float2 (&acc)[4]) {
   const float4* wv = reinterpret_cast<const float4*>(w);
-  float2 a2 = make_float2(0.f, 0.f);
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     const float4 wj = wv[j];
     const float x0 = __uint_as_float(x[4 * j + 0]), x1 = __uint_as_float(x[4 * j + 1]);
     const float x2 = __uint_as_float(x[4 * j + 2]), x3 = __uint_as_float(x[4 * j + 3]);
-    acc = ffma2(make_float2(wj.x, wj.y), make_float2(fmaxf(x0, 0.f), x1 + fabsf(x1)), acc);
-    a2 = ffma2(make_float2(wj.z, wj.w), make_float2(fmaxf(x2, 0.f), x3 + fabsf(x3)), a2);
+    float2& a0 = acc[(2 * j) & 3];
+    float2& a1 = acc[(2 * j + 1) & 3];
+    a0 = __ffma2_rn(make_float2(wj.x, wj.y), make_float2(fmaxf(x0, 0.f), x1 + fabsf(x1)), a0);
+    a1 = __ffma2_rn(make_float2(wj.z, wj.w), make_float2(fmaxf(x2, 0.f), x3 + fabsf(x3)), a1);
   }
-  acc.x += a2.x;
-  acc.y += a2.y;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -187,10 +177,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(q_full(b), 1);
       mbar_init(q_empty(b), 1);
       mbar_init(acc_full(b), 1);
-      mbar_init(acc_empty(b), 8 * 32);
+      mbar_init(acc_empty(b), kEpiGroups * 128);
     }
     mbar_init(drain_bar, 1);
-    for (int b = 0; b < 4; ++b) mbar_init(w_full(b >> 1, b & 1), 128);
+    for (int b = 0; b < 2 * kEpiGroups; ++b) mbar_init(w_full(b >> 1, b & 1), 128);
     *abort_flag = 0;
     fence_mbar_init();
     fence_proxy_async_smem();
@@ -272,7 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ epilogue
-    const int e = (warp - 4) >> 2;         // warpgroup: tokens 2e, 2e+1
+    const int e = (warp - 4) >> 2;         // warpgroup: token e of the item
     const int wq = warp & 3;               // TMEM lane quarter of this warp
     const int et = threadIdx.x - 128 - e * 128;
     Walker wk;
@@ -281,65 +271,45 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int64_t it = blockIdx.x; ok && wk.seek(it, P, item); it += gridDim.x) {
       if (item.kt0 >= item.kt1) continue;
-      float* wsm = wbuf + (qi & 1) * (kMaxTokens * kHeads);
-      {
-        const int g = 2 * e + (et >> 6), j = et & 63;
-        if (g < item.g) {
-          const int64_t t = item.t0 + g;
-          // odd heads are pre-halved: their ReLU is taken as x + |x| = 2 ReLU(x)
-          wsm[g * kHeads + j] = __ldg(P.w + t * kHeads + j) * (P.q_scale ? __ldg(P.q_scale + t) : 1.f) *
-                                ((j & 1) ? 0.5f : 1.f);
-        }
+      float* wsm = wbuf + (qi & 1) * (kMaxTokens * kHeads) + e * kHeads;
+      const bool have = e < item.g;        // this warpgroup's token exists in the item
+      if (have && et < kHeads) {
+        const int64_t t = item.t0 + e;
+        // odd heads are pre-halved: their ReLU is taken as x + |x| = 2 ReLU(x)
+        wsm[et] = __ldg(P.w + t * kHeads + et) * (P.q_scale ? __ldg(P.q_scale + t) : 1.f) *
+                  ((et & 1) ? 0.5f : 1.f);
       }
       mbar_arrive(w_full(e, qi & 1));
       if (!warp_wait(w_full(e, qi & 1), (qi >> 1) & 1, abort_flag)) break;
       ++qi;
-      const int ng = item.g - 2 * e;       // tokens of this warpgroup (may be <= 0)
+      const int64_t srow = item.t0 + e - P.row_begin;   // score row of this token
+      const int plim = item.pos0 + e;                    // its last candidate
       for (int kt = item.kt0; kt < item.kt1; ++kt, ++ti) {
         const int ab = ti & 1;
         if (!warp_wait(acc_full(ab), (ti >> 1) & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
-        // Columns of this warpgroup: token 2e at [0, 64), token 2e+1 at [64, 128)
-        // (relative to ta), read in 32-column chunks.
-        const uint32_t ta = tmem + (static_cast<uint32_t>(wq * 32) << 16) + ab * kAccCols + e * 128;
-        const int nchunk = ng >= 2 ? 4 : (ng == 1 ? 2 : 0);
-        const int s = kt * kKeys + wq * 32 + lane;   // sequence-local key of this thread
-        const int pmax = item.pos0 + item.g - 1;
-        const float ks = (s <= pmax && P.k_scale) ? __ldg(P.k_scale + item.kv0 + s) : 1.f;
-        // token 2e in chunks 0-1, token 2e+1 in chunks 2-3; chunk c+1 is loaded
-        // while chunk c is reduced
-        float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-        const float* wg = wsm + (2 * e) * kHeads;
-        auto release = [&]() {
+        if (!have) {
           tc_fence_before();
-          mbar_arrive(acc_empty(ab));   // accumulator fully read: the MMA may reuse it
-        };
-        if (nchunk == 0) {
-          release();
-        } else {
-          uint32_t xa[32], xb[32];
-          tmem_ld32(ta, xa);
-          tmem_wait_ld();
-          tmem_ld32(ta + 32, xb);
-          reduce_chunk(xa, wg, acc[0]);
-          tmem_wait_ld();
-          if (nchunk == 4) tmem_ld32(ta + 64, xa); else release();
-          reduce_chunk(xb, wg + 32, acc[0]);
-          if (nchunk == 4) {
-            tmem_wait_ld();
-            tmem_ld32(ta + 96, xb);
-            reduce_chunk(xa, wg + 64, acc[1]);
-            tmem_wait_ld();
-            release();
-            reduce_chunk(xb, wg + 96, acc[1]);
-          }
+          mbar_arrive(acc_empty(ab));
+          continue;
         }
+        // token e at columns [64e, 64e + 64) of the accumulator
+        const uint32_t ta = tmem + (static_cast<uint32_t>(wq * 32) << 16) + ab * kAccCols + e * kHeads;
+        const int s = kt * kKeys + wq * 32 + lane;   // sequence-local key of this thread
+        const float ks = (s <= plim && P.k_scale) ? __ldg(P.k_scale + item.kv0 + s) : 1.f;
+        uint32_t xa[32], xb[32];
+        tmem_ld32(ta, xa);
+        tmem_ld32(ta + 32, xb);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(acc_empty(ab));      // accumulator read: the MMA may reuse it
+        float2 acc[4];
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int g = 2 * e + u;
-          if (u < ng && s <= item.pos0 + g)
-            P.scores[(item.t0 + g - P.row_begin) * P.ld + s] = (acc[u].x + acc[u].y) * ks;
-        }
+        for (int v = 0; v < 4; ++v) acc[v] = make_float2(0.f, 0.f);
+        reduce_chunk(xa, wsm, acc);
+        reduce_chunk(xb, wsm + 32, acc);
+        const float2 t = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
+        if (s <= plim) P.scores[srow * P.ld + s] = (t.x + t.y) * ks;
       }
     }
   }
