@@ -48,7 +48,9 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=2)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle cpu_baseline leg")
-    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target oracle time per sample")
+    ap.add_argument("--cpu-seconds", type=float, default=25.0, help="target oracle time per sample")
+    ap.add_argument("--decode-steps", type=int, default=10,
+                    help="timed steps of the ragged 128K decode measurement (0 = skip)")
     return ap.parse_args()
 
 
@@ -90,14 +92,37 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+KERNEL_SOURCES = {"mla_tc": "mla_tc.cuh", "indexer_tc": "indexer_tc.cuh", "topk": "topk.cuh"}
+
+
+def kernel_source_sha(name):
+    """sha256 of the kernel's source file plus the shared headers: traffic
+    counters taken on another version of the kernel are not reused."""
+    import hashlib
+    csrc = os.path.join(ROOT, "sparse_long_context_07_b300", "csrc")
+    h = hashlib.sha256()
+    for f in (KERNEL_SOURCES.get(name, ""), "ptx.cuh", "common.cuh"):
+        p = os.path.join(csrc, f)
+        if f and os.path.exists(p):
+            with open(p, "rb") as fh:
+                h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
 def load_traffic():
-    """DRAM traffic per unit of work from the committed ncu summary, if any."""
+    """DRAM bytes per launch from the committed ncu summary, for kernels whose
+    source still matches the one the counters were taken on."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(p) as f:
-            return json.load(f)
+            tab = json.load(f)
     except Exception:
         return {}
+    out = {}
+    for name, ent in tab.items():
+        if isinstance(ent, dict) and ent.get("source_sha") == kernel_source_sha(name):
+            out[name] = {k: v for k, v in ent.items() if k != "source_sha"}
+    return out
 
 
 # ----------------------------------------------------------------------------
@@ -299,6 +324,12 @@ def main():
     if not a.no_e2e:
         e2e = measure_e2e(a, wl, dsa, b, ix, m, out, lse, ws, stream, world, dev)
 
+    decode = None
+    if a.decode_steps > 0 and a.workload != "ragged128k":
+        del out, lse, ws
+        torch.cuda.empty_cache()
+        decode = measure_decode(a, dsa, dev, stream)
+
     if rank != 0:
         return
     cpu = None
@@ -330,6 +361,7 @@ def main():
         "e2e": e2e,
         "gpu_launches": launches,
         "clocks": clk,
+        "decode": decode,
     }
     print(json.dumps(line))
 
@@ -376,6 +408,65 @@ def roofline(wl, per_kernel, steps):
     res.update({"achieved": achieved, "peak": peak, "frac": achieved / peak,
                 "traffic": (tr * nl / steps / max(1, nl / steps)) if tr else None,
                 "launches_per_step": nl / steps, "ms_per_step": tot_ms / steps})
+    return res
+
+
+def measure_decode(a, dsa, dev, stream):
+    """Secondary measurement: one decode step of 64 sequences with 16K-128K
+    cached tokens each (1 query token per sequence), L2 flushed before every
+    timed step; reports tokens/s and the HBM fraction of the sparse attention
+    and of the indexer (both bandwidth-bound in decode)."""
+    import torch
+    import dsa_synth
+    wl = dsa_synth.WORKLOADS["ragged128k"](device=dev)
+    b = dsa.Batch(wl.cu_q, wl.cu_kv, wl.seqlens_q, wl.seqlens_kv)
+    ix = dsa.Indexer(wl.q_idx, wl.k_idx, wl.w, wl.q_scale, wl.k_scale)
+    m = dsa.Mla(wl.Q, wl.KV, wl.scale, wl.d_v)
+    T, k = wl.total_q, wl.topk
+    out = torch.empty((T, wl.n_heads, wl.d_v), dtype=wl.Q.dtype, device=dev)
+    lse = torch.empty((T, wl.n_heads), dtype=torch.float32, device=dev)
+    _, pref = dsa.workspace_size(b, ix, m, k)
+    ws = torch.empty(pref, dtype=torch.uint8, device=dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)   # 512 MiB > L2
+    for _ in range(3):
+        dsa.forward(b, ix, m, k, out, lse, None, ws, stream=stream)
+    torch.cuda.synchronize()
+    totals, per_kernel = [], {}
+    for _ in range(a.decode_steps):
+        flush.fill_(1)
+        tr = dsa.Trace(capacity=64)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        dsa.forward(b, ix, m, k, out, lse, None, ws, stream=stream, trace=tr)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        totals.append(e0.elapsed_time(e1))
+        for name, t in tr.launches():
+            per_kernel.setdefault(name, []).append(t)
+    if dsa.read_device_errors() != 0:
+        raise RuntimeError("device error word set during the decode measurement")
+    peaks, src = load_peaks()
+    ms = statistics.median(totals)
+    kms = {kname: statistics.median(v) for kname, v in per_kernel.items()}
+    nkv = np.asarray(wl.seqlens_kv, dtype=np.float64)
+    kk = np.minimum(nkv, k)
+    # algorithmic bytes: indexer reads every candidate key (128 B + 4 B scale) and
+    # the query (8 KiB + 256 B weights + scale); sparse MLA gathers the selected
+    # latent rows and reads Q, writes out, reads the indices
+    idx_bytes = float((nkv * (wl.idx_dim + 4)).sum() + T * (wl.n_idx_heads * wl.idx_dim + 4 * wl.n_idx_heads + 4))
+    mla_bytes = float((kk * wl.d_qk * 2).sum() + T * (wl.n_heads * wl.d_qk * 2 + wl.n_heads * wl.d_v * 2 + 4 * k))
+    mla_ms = kms.get("mla_tc", 0.0) + kms.get("mla_combine", 0.0)
+    res = {"workload": wl.name, "tokens_per_step": T, "ms_per_step": ms, "value": T / (ms / 1e3),
+           "unit": "tokens/s", "steps": a.decode_steps, "l2": "flushed before every step (512 MiB write)",
+           "kernels_ms_per_step": kms}
+    if mla_ms > 0:
+        gbs = mla_bytes / (mla_ms / 1e3) / 1e9
+        res["mla_hbm"] = {"achieved": gbs, "peak": peaks.get("hbm_gbs"), "unit": "GB/s",
+                          "frac": gbs / peaks.get("hbm_gbs"), "bytes": mla_bytes, "note": f"{src} copy bandwidth"}
+    if kms.get("indexer_tc"):
+        gbs = idx_bytes / (kms["indexer_tc"] / 1e3) / 1e9
+        res["indexer_hbm"] = {"achieved": gbs, "peak": peaks.get("hbm_gbs"), "unit": "GB/s",
+                              "frac": gbs / peaks.get("hbm_gbs"), "bytes": idx_bytes}
     return res
 
 

@@ -213,7 +213,8 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(
   }
 
   // ---- pass 2: bins above b* are selected, bin b* keeps candidates
-  for (int i = tid; i < kBitmapWords; i += kThreads) { sm.sel[i] = 0u; sm.tie[i] = 0u; }
+  const int nwords = (n + 31) >> 5;
+  for (int i = tid; i < nwords; i += kThreads) { sm.sel[i] = 0u; sm.tie[i] = 0u; }
   if (tid == 0) sm.ncand = 0u;
   __syncthreads();
   auto classify = [&](float x, int i) {
@@ -264,7 +265,6 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(
   __syncthreads();
 
   // ---- ordered emission: thread t scans bitmap words [8t, 8t+8)
-  const int nwords = (n + 31) >> 5;
   const int w0 = tid * kWordsPerThread;
   uint32_t sel_cnt = 0, tie_cnt = 0;
 #pragma unroll
