@@ -192,8 +192,9 @@ dsa_status_t dsa_sparse_mla(const dsa_batch_t* batch, const dsa_mla_t* mla, cons
  * results and errors as dsa_sparse_mla, minus ws/ws_bytes: the split-KV
  * partials of small decode batches live in a 24 MiB array compiled into the
  * library, which every GPU that loads the library holds until the process
- * exits.  A batch whose split plan needs more than 24 MiB (decode batches of
- * roughly 21 to 73 query rows) is rejected with DSA_ERROR_NOT_SUPPORTED;
+ * exits.  A batch whose split plan needs more than 24 MiB (on a 148-SM B300
+ * with k = 2048: decode batches of 24 or of 32 to 36 query rows) is rejected
+ * with DSA_ERROR_NOT_SUPPORTED;
  * call dsa_sparse_mla with a workspace for those.  The first call on each
  * device looks up the array's device address (cudaGetSymbolAddress), so make
  * that first call before any stream capture.  Every call shares the one

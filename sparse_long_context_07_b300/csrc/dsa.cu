@@ -298,15 +298,16 @@ struct MlaPlan {
 };
 
 // Each (row, split) unit runs on two CTAs (one per half of the output
-// columns).  Fewer units than half the SMs leave SMs idle, so each row's
-// selected tiles are then split over several units (partials merged by the
-// combine kernel).
+// columns).  When the rows alone would leave more than half of the SMs idle,
+// each row's selected tiles are split over several units (partials merged by
+// the combine kernel); a split costs a second wave and a second per-CTA
+// start-up, so it is not taken for a mostly full wave.
 // The split count shrinks until its scratch fits `ws_cap` bytes.
 MlaPlan plan_mla(int sms, int64_t rows, int32_t k, size_t ws_cap = SIZE_MAX) {
   const int tiles = (k + dsa::mla_tc::kRows - 1) / dsa::mla_tc::kRows;
   const int64_t units_wanted = std::max(1, sms / 2);
   int want = 1;
-  if (rows < units_wanted) want = static_cast<int>((units_wanted + rows - 1) / rows);
+  if (2 * rows < units_wanted) want = static_cast<int>((units_wanted + rows - 1) / rows);
   want = std::min(want, tiles);
   for (;; --want) {
     MlaPlan p;

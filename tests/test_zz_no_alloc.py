@@ -51,7 +51,7 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls():
 
 def test_noalloc_refuses_batches_beyond_its_scratch():
     k = 2048
-    wl = _decode_batch([4096] * 64, seed=42)   # 64 rows x 2 splits of fp32 partials > 24 MiB
+    wl = _decode_batch([4096] * 34, seed=42)   # 34 rows x 3 splits of fp32 partials > 24 MiB
     b, _, m = structs(wl)
     idx = random_selection(wl, k, seed=7).cuda()
     out = torch.empty((wl.total_q, wl.n_heads, wl.d_v), dtype=torch.bfloat16, device="cuda")
