@@ -19,9 +19,11 @@
 //   warp 0      TMA producer: q block of the item, then a ring of key tiles
 //   warp 1      MMA issuer (one thread): 4 x tcgen05.mma kind::f8f6f4 per tile
 //   warp 2      TMEM allocator
-//   warps 4-19  four epilogue warpgroups; warpgroup e handles token e
-// Two TMEM accumulators (2 x 256 columns) let the epilogue of tile i overlap
-// the MMA of tile i+1.
+//   warps 4-19  four epilogue warpgroups; warpgroup e handles column group e
+// Two TMEM accumulator slots (2 x 256 columns) let the epilogue of one slot
+// overlap the MMAs of the next.  A slot holds four 64-column groups: for an
+// item of g query rows, 4/g consecutive key tiles (one for g >= 3), so the
+// four epilogue warpgroups share the work also in decode (g = 1).
 //
 // Work items: a group of up to G consecutive query rows of one sequence (from
 // the last rows backwards, so long causal rows start first) and a chunk of at
@@ -127,6 +129,12 @@ struct Walker {
   }
 };
 
+// Key tiles packed into one 256-column accumulator slot for an item of g
+// query rows: a slot holds 4 column groups of 64 (token, key tile) pairs, so
+// an item of one row (decode) fills a slot with 4 consecutive key tiles and
+// all four epilogue warpgroups work on it.
+__device__ __forceinline__ int tiles_per_slot(int g) { return g >= 3 ? 1 : 4 / g; }
+
 // acc += sum_j w[j] ReLU(x[j]) over 32 heads.  Even heads take ReLU as
 // max(x, 0) (ALU pipe), odd heads as x + |x| = 2 ReLU(x) (FMA pipe) against
 // weights staged at half value; both products then share one packed fp32x2
@@ -231,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       Walker wk;
       Item item;
-      int qi = 0, ti = 0;
+      int qi = 0, ti = 0, si = 0;   // q blocks, key tiles, accumulator slots
       bool ok = true;
       for (int64_t it = blockIdx.x; ok && wk.seek(it, P, item); it += gridDim.x) {
         if (item.kt0 >= item.kt1) continue;
@@ -240,17 +248,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t idesc = make_idesc(0, 0, kKeys, kHeads * item.g, 0, 0);
         const uint32_t qaddr = sbase + kOffQ + qb * kQBytes;
-        for (int kt = item.kt0; kt < item.kt1; ++kt, ++ti) {
-          const int st = ti % kStages, ab = ti & 1;
-          if (ti >= 2 && !mbar_wait(acc_empty(ab), ((ti >> 1) - 1) & 1, abort_flag)) { ok = false; break; }
-          if (!mbar_wait(kv_full(st), (ti / kStages) & 1, abort_flag)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t kaddr = sbase + kOffK + st * kTileBytes;
+        const int per = tiles_per_slot(item.g);
+        if (per == 1) {
+          // one key tile per slot (items of 3 or 4 rows)
+          for (int kt = item.kt0; kt < item.kt1; ++kt, ++ti, ++si) {
+            const int st = ti % kStages, ab = si & 1;
+            if (si >= 2 && !mbar_wait(acc_empty(ab), ((si >> 1) - 1) & 1, abort_flag)) { ok = false; break; }
+            if (!mbar_wait(kv_full(st), (ti / kStages) & 1, abort_flag)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t kaddr = sbase + kOffK + st * kTileBytes;
 #pragma unroll
-          for (int ks = 0; ks < kDim / 32; ++ks)
-            mma_fp8(tmem + ab * kAccCols, make_desc_sw128(kaddr + ks * 32, 16, 1024),
-                    make_desc_sw128(qaddr + ks * 32, 16, 1024), idesc, ks > 0 ? 1u : 0u);
-          mma_commit(kv_empty(st));
+            for (int ks = 0; ks < kDim / 32; ++ks)
+              mma_fp8(tmem + ab * kAccCols, make_desc_sw128(kaddr + ks * 32, 16, 1024),
+                      make_desc_sw128(qaddr + ks * 32, 16, 1024), idesc, ks > 0 ? 1u : 0u);
+            mma_commit(kv_empty(st));
+            mma_commit(acc_full(ab));
+          }
+        } else
+        for (int kt = item.kt0; kt < item.kt1 && ok; kt += per, ++si) {
+          const int ab = si & 1;
+          if (si >= 2 && !mbar_wait(acc_empty(ab), ((si >> 1) - 1) & 1, abort_flag)) { ok = false; break; }
+          for (int u = 0; u < per && kt + u < item.kt1; ++u, ++ti) {
+            const int st = ti % kStages;
+            if (!mbar_wait(kv_full(st), (ti / kStages) & 1, abort_flag)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t kaddr = sbase + kOffK + st * kTileBytes;
+            const uint32_t dcol = ab * kAccCols + u * kHeads * item.g;
+#pragma unroll
+            for (int ks = 0; ks < kDim / 32; ++ks)
+              mma_fp8(tmem + dcol, make_desc_sw128(kaddr + ks * 32, 16, 1024),
+                      make_desc_sw128(qaddr + ks * 32, 16, 1024), idesc, ks > 0 ? 1u : 0u);
+            mma_commit(kv_empty(st));
+          }
+          if (!ok) break;
           mma_commit(acc_full(ab));
         }
         if (!ok) break;
@@ -262,19 +292,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ epilogue
-    const int e = (warp - 4) >> 2;         // warpgroup: token e of the item
+    const int e = (warp - 4) >> 2;         // warpgroup: column group e of each slot
     const int wq = warp & 3;               // TMEM lane quarter of this warp
     const int et = threadIdx.x - 128 - e * 128;
     Walker wk;
     Item item;
-    int qi = 0, ti = 0;
+    int qi = 0, si = 0;
     bool ok = true;
     for (int64_t it = blockIdx.x; ok && wk.seek(it, P, item); it += gridDim.x) {
       if (item.kt0 >= item.kt1) continue;
+      // column group e of a slot: key tile u = e / g of the slot, token e % g
+      const int per = tiles_per_slot(item.g);
+      const int u = e / item.g, te = e % item.g;
+      const bool used = u < per;
       float* wsm = wbuf + (qi & 1) * (kMaxTokens * kHeads) + e * kHeads;
-      const bool have = e < item.g;        // this warpgroup's token exists in the item
-      if (have && et < kHeads) {
-        const int64_t t = item.t0 + e;
+      if (used && et < kHeads) {
+        const int64_t t = item.t0 + te;
         // odd heads are pre-halved: their ReLU is taken as x + |x| = 2 ReLU(x)
         wsm[et] = __ldg(P.w + t * kHeads + et) * (P.q_scale ? __ldg(P.q_scale + t) : 1.f) *
                   ((et & 1) ? 0.5f : 1.f);
@@ -282,19 +315,51 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(w_full(e, qi & 1));
       if (!warp_wait(w_full(e, qi & 1), (qi >> 1) & 1, abort_flag)) break;
       ++qi;
-      const int64_t srow = item.t0 + e - P.row_begin;   // score row of this token
-      const int plim = item.pos0 + e;                    // its last candidate
-      for (int kt = item.kt0; kt < item.kt1; ++kt, ++ti) {
-        const int ab = ti & 1;
-        if (!warp_wait(acc_full(ab), (ti >> 1) & 1, abort_flag)) { ok = false; break; }
+      const int64_t srow = item.t0 + te - P.row_begin;   // score row of this token
+      const int plim = item.pos0 + te;                    // its last candidate
+      if (per == 1) {
+        // one key tile per slot (items of 3 or 4 rows): token e at columns
+        // [64e, 64e + 64)
+        for (int kt = item.kt0; kt < item.kt1; ++kt, ++si) {
+          const int ab = si & 1;
+          if (!warp_wait(acc_full(ab), (si >> 1) & 1, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          if (!used) {
+            tc_fence_before();
+            mbar_arrive(acc_empty(ab));
+            continue;
+          }
+          const uint32_t ta = tmem + (static_cast<uint32_t>(wq * 32) << 16) + ab * kAccCols + e * kHeads;
+          const int s = kt * kKeys + wq * 32 + lane;   // sequence-local key of this thread
+          const float ks = (s <= plim && P.k_scale) ? __ldg(P.k_scale + item.kv0 + s) : 1.f;
+          uint32_t xa[32], xb[32];
+          tmem_ld32(ta, xa);
+          tmem_ld32(ta + 32, xb);
+          tmem_wait_ld();
+          tc_fence_before();
+          mbar_arrive(acc_empty(ab));      // accumulator read: the MMA may reuse it
+          float2 acc[4];
+#pragma unroll
+          for (int v = 0; v < 4; ++v) acc[v] = make_float2(0.f, 0.f);
+          reduce_chunk(xa, wsm, acc);
+          reduce_chunk(xb, wsm + 32, acc);
+          const float2 tt = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
+          if (s <= plim) P.scores[srow * P.ld + s] = (tt.x + tt.y) * ks;
+        }
+        continue;
+      }
+      for (int kt0 = item.kt0; kt0 < item.kt1; kt0 += per, ++si) {
+        const int ab = si & 1;
+        if (!warp_wait(acc_full(ab), (si >> 1) & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
-        if (!have) {
+        const int kt = kt0 + u;
+        if (!used || kt >= item.kt1) {
           tc_fence_before();
           mbar_arrive(acc_empty(ab));
           continue;
         }
-        // token e at columns [64e, 64e + 64) of the accumulator
-        const uint32_t ta = tmem + (static_cast<uint32_t>(wq * 32) << 16) + ab * kAccCols + e * kHeads;
+        const uint32_t ta = tmem + (static_cast<uint32_t>(wq * 32) << 16) + ab * kAccCols +
+                            u * kHeads * item.g + te * kHeads;
         const int s = kt * kKeys + wq * 32 + lane;   // sequence-local key of this thread
         const float ks = (s <= plim && P.k_scale) ? __ldg(P.k_scale + item.kv0 + s) : 1.f;
         uint32_t xa[32], xb[32];
@@ -308,8 +373,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int v = 0; v < 4; ++v) acc[v] = make_float2(0.f, 0.f);
         reduce_chunk(xa, wsm, acc);
         reduce_chunk(xb, wsm + 32, acc);
-        const float2 t = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
-        if (s <= plim) P.scores[srow * P.ld + s] = (t.x + t.y) * ks;
+        const float2 tt = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
+        if (s <= plim) P.scores[srow * P.ld + s] = (tt.x + tt.y) * ks;
       }
     }
   }
