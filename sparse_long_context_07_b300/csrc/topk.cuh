@@ -193,8 +193,22 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(
   __syncthreads();
   const int n4 = n >> 2;
   const float4* __restrict__ row4 = reinterpret_cast<const float4*>(row);
-  for (int i = tid; i < n4; i += kThreads) {
-    const float4 v = __ldg(row4 + i);
+  // four 16-byte loads in flight per thread
+  int i4 = tid;
+  for (; i4 + 3 * kThreads < n4; i4 += 4 * kThreads) {
+    float4 v[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) v[q] = __ldg(row4 + i4 + q * kThreads);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      atomicAdd(&sm.hist[order_key(v[q].x) >> 21], 1u);
+      atomicAdd(&sm.hist[order_key(v[q].y) >> 21], 1u);
+      atomicAdd(&sm.hist[order_key(v[q].z) >> 21], 1u);
+      atomicAdd(&sm.hist[order_key(v[q].w) >> 21], 1u);
+    }
+  }
+  for (; i4 < n4; i4 += kThreads) {
+    const float4 v = __ldg(row4 + i4);
     atomicAdd(&sm.hist[order_key(v.x) >> 21], 1u);
     atomicAdd(&sm.hist[order_key(v.y) >> 21], 1u);
     atomicAdd(&sm.hist[order_key(v.z) >> 21], 1u);
@@ -228,9 +242,20 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(
       sm.cand_idx[slot] = i;
     }
   };
-  for (int i = tid; i < n4; i += kThreads) {
-    const float4 v = __ldg(row4 + i);
-    classify(v.x, 4 * i); classify(v.y, 4 * i + 1); classify(v.z, 4 * i + 2); classify(v.w, 4 * i + 3);
+  i4 = tid;
+  for (; i4 + 3 * kThreads < n4; i4 += 4 * kThreads) {
+    float4 v[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) v[q] = __ldg(row4 + i4 + q * kThreads);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int i = i4 + q * kThreads;
+      classify(v[q].x, 4 * i); classify(v[q].y, 4 * i + 1); classify(v[q].z, 4 * i + 2); classify(v[q].w, 4 * i + 3);
+    }
+  }
+  for (; i4 < n4; i4 += kThreads) {
+    const float4 v = __ldg(row4 + i4);
+    classify(v.x, 4 * i4); classify(v.y, 4 * i4 + 1); classify(v.z, 4 * i4 + 2); classify(v.w, 4 * i4 + 3);
   }
   for (int i = 4 * n4 + tid; i < n; i += kThreads) classify(__ldg(row + i), i);
   __syncthreads();
