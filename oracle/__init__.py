@@ -14,6 +14,8 @@ matmul, exp/log, and lexsort.
 
 from .dsa_oracle import (  # noqa: F401
     decode_e4m3,
+    encode_e4m3,
+    quantize_e4m3_groups,
     decode_bf16,
     query_positions,
     index_scores_row,

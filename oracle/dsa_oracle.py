@@ -61,6 +61,76 @@ def decode_e4m3(codes: np.ndarray) -> np.ndarray:
     return out
 
 
+def encode_e4m3(values: np.ndarray) -> np.ndarray:
+    """Encode float values to OCP E4M3 bytes [OCP, E4M3], rounding to nearest
+    with ties to even and saturating at the largest finite magnitude, 448.
+
+    The values are taken exactly (float64 holds every float32).  Normal codes
+    are 2^(e-7) * (1 + m/8) for e = 1..15 (e = 15 with m = 7 is NaN, so the
+    top finite value is 2^8 * 1.75 = 448); subnormals are 2^-6 * m/8.  A value
+    is rounded on the grid of its binade: step 2^(E-3) for |v| in [2^E, 2^(E+1))
+    with E >= -6, step 2^-9 below 2^-6.  -0.0 encodes as 0x80.
+    """
+    v = np.asarray(values, dtype=np.float64)
+    out = np.zeros(v.shape, dtype=np.uint8)
+    flat_v = v.reshape(-1)
+    flat_o = out.reshape(-1)
+    for i, x in enumerate(flat_v):
+        sign = 0x80 if np.signbit(x) else 0x00
+        a = abs(float(x))
+        if a >= 448.0:
+            flat_o[i] = sign | 0x7E
+            continue
+        if a < 2.0 ** -6:
+            step = 2.0 ** -9                    # subnormal grid (and the first normal)
+        else:
+            E = int(np.floor(np.log2(a)))
+            # guard the floor of log2 at exact powers of two
+            if 2.0 ** E > a:
+                E -= 1
+            elif 2.0 ** (E + 1) <= a:
+                E += 1
+            step = 2.0 ** (E - 3)
+        q = a / step                            # exact: step is a power of two
+        n = np.floor(q)
+        r = q - n
+        if r > 0.5 or (r == 0.5 and int(n) % 2 == 1):
+            n += 1
+        y = n * step                            # the rounded magnitude
+        if y >= 448.0:
+            flat_o[i] = sign | 0x7E
+            continue
+        if y < 2.0 ** -6:
+            code = int(round(y / 2.0 ** -9))    # subnormal m (0..7)
+        else:
+            E = int(np.floor(np.log2(y)))
+            if 2.0 ** E > y:
+                E -= 1
+            elif 2.0 ** (E + 1) <= y:
+                E += 1
+            m = int(round((y / 2.0 ** E - 1.0) * 8.0))
+            code = ((E + 7) << 3) | m
+        flat_o[i] = sign | code
+    return out
+
+
+def quantize_e4m3_groups(x32: np.ndarray, group_elems: int):
+    """Per-group absmax quantisation to E4M3 (the format of the indexer
+    inputs, "FP8" [P1 §3.1], one fp32 scale per group): for each group of
+    `group_elems` consecutive values, scale = amax / 448 in fp32 (1 when
+    amax = 0) and code = E4M3(x / scale), the division done in fp32 -- the
+    precision in which the kernel takes the same decision -- then rounded to
+    nearest even with saturation.  x32: float32 array whose size is a multiple
+    of group_elems.  Returns (uint8 codes of x's shape, float32 scales)."""
+    x = np.asarray(x32, dtype=np.float32)
+    g = x.reshape(-1, group_elems)
+    amax = np.abs(g).max(axis=1)
+    scale = np.where(amax > 0, amax / np.float32(448.0), np.float32(1.0)).astype(np.float32)
+    y = (g / scale[:, None]).astype(np.float32)     # IEEE fp32 division
+    codes = encode_e4m3(y).reshape(x.shape)
+    return codes, scale
+
+
 def decode_bf16(bits: np.ndarray) -> np.ndarray:
     """Decode bfloat16 bit patterns (uint16) to float64: a bf16 value is the
     upper half of the float32 with the same bits."""

@@ -53,6 +53,74 @@ def test_bf16_decode_matches_library():
     assert oracle.decode_bf16(np.array([0xC040], np.uint16))[0] == -3.0
 
 
+def test_e4m3_encode_round_trips_every_finite_code():
+    codes = np.arange(256, dtype=np.uint8)
+    vals = oracle.decode_e4m3(codes)
+    fin = ~np.isnan(vals)
+    assert np.array_equal(oracle.encode_e4m3(vals[fin]), codes[fin])
+
+
+def _e4m3_midpoint_cases():
+    # each pair of adjacent finite codes of one sign, the value halfway between
+    # them, and the code round-to-nearest-even picks (even mantissa field)
+    vals = oracle.decode_e4m3(np.arange(0x7F, dtype=np.uint8))
+    out = []
+    for c in range(0x7E):
+        lo, hi = vals[c], vals[c + 1]
+        out.append(((lo + hi) / 2.0, c if (c & 1) == 0 else c + 1))
+    return out
+
+
+def test_e4m3_encode_ties_to_even_and_nearest():
+    for mid, want in _e4m3_midpoint_cases():
+        assert int(oracle.encode_e4m3(np.array([mid]))[0]) == want, mid
+        assert int(oracle.encode_e4m3(np.array([-mid]))[0]) == want | 0x80, mid
+    # just off the midpoint goes to the nearer neighbour
+    v = oracle.decode_e4m3(np.array([0x38, 0x39], np.uint8))   # 1.0, 1.125
+    assert oracle.encode_e4m3(np.array([1.0625 + 1e-9]))[0] == 0x39
+    assert oracle.encode_e4m3(np.array([1.0625 - 1e-9]))[0] == 0x38
+    assert v[0] == 1.0 and v[1] == 1.125
+
+
+def test_e4m3_encode_saturates_and_keeps_signed_zero():
+    enc = lambda x: int(oracle.encode_e4m3(np.array([x]))[0])
+    assert enc(448.0) == 0x7E and enc(-448.0) == 0xFE
+    assert enc(460.0) == 0x7E and enc(1e30) == 0x7E and enc(-1e30) == 0xFE
+    assert enc(0.0) == 0x00 and enc(-0.0) == 0x80
+    assert enc(2.0 ** -10) == 0x00          # half the smallest subnormal: tie to even (0)
+    assert enc(3 * 2.0 ** -10) == 0x02      # 1.5 subnormal steps: tie to even (2)
+
+
+def test_e4m3_encode_matches_library_cast():
+    # torch's float8_e4m3fn cast (round to nearest even) on values inside the
+    # finite range: an independent implementation of the same encoding
+    rng = np.random.default_rng(1)
+    x = rng.standard_normal(30000) * rng.choice([1e-5, 1e-3, 0.1, 1.0, 40.0, 300.0], 30000)
+    x = np.clip(x, -448.0, 448.0).astype(np.float32)
+    lib = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(oracle.encode_e4m3(x), lib)
+
+
+def test_quantize_groups_scale_and_extremes():
+    rng = np.random.default_rng(2)
+    x = (rng.standard_normal((7, 96)) * rng.uniform(0.01, 50, (7, 1))).astype(np.float32)
+    x[3] = 0.0                               # an all-zero group
+    codes, scale = oracle.quantize_e4m3_groups(x, 96)
+    assert codes.shape == x.shape and scale.dtype == np.float32
+    amax = np.abs(x).max(axis=1)
+    for g in range(7):
+        if amax[g] == 0:
+            assert scale[g] == 1.0 and not codes[g].any()
+            continue
+        assert scale[g] == np.float32(amax[g] / np.float32(448.0))
+        j = int(np.argmax(np.abs(x[g])))
+        assert codes[g, j] in (0x7E, 0xFE)   # the extreme value lands on +-448
+        deq = oracle.decode_e4m3(codes[g]) * float(scale[g])
+        # e4m3 keeps 3 mantissa bits: relative error <= 2^-4 above the subnormals
+        big = np.abs(x[g]) >= 2.0 ** -6 * float(scale[g])
+        assert np.all(np.abs(deq[big] - x[g][big]) <= 2.0 ** -4 * np.abs(x[g][big]) + 1e-30)
+
+
 # --------------------------------------------------------------------------
 # Batch geometry
 # --------------------------------------------------------------------------
@@ -350,3 +418,48 @@ def test_mutant_topk_fails_pin(bad):
 def test_mutant_attention_fails_pin(bad):
     # value-column mistake fails the closed form; scale mistake fails it too
     assert not check_attention_closed_form(bad)
+
+
+def check_e4m3_encoder(enc) -> bool:
+    """The encoder pins (round trip, midpoints, saturation) as one predicate."""
+    codes = np.arange(256, dtype=np.uint8)
+    vals = oracle.decode_e4m3(codes)
+    fin = ~np.isnan(vals)
+    if not np.array_equal(enc(vals[fin]), codes[fin]):
+        return False
+    for mid, want in _e4m3_midpoint_cases():
+        if int(enc(np.array([mid]))[0]) != want:
+            return False
+    return int(enc(np.array([460.0]))[0]) == 0x7E and int(enc(np.array([1e6]))[0]) == 0x7E
+
+
+def _enc_ties_away(v):
+    # rounds halfway cases away from zero: nudge every value up by a hair
+    v = np.asarray(v, dtype=np.float64)
+    return oracle.encode_e4m3(v * (1 + 1e-12))
+
+
+def _enc_truncate(v):
+    # rounds toward zero: the nearest code not above |v|
+    v = np.asarray(v, dtype=np.float64)
+    grid = oracle.decode_e4m3(np.arange(0x7F, dtype=np.uint8))
+    out = np.searchsorted(grid, np.abs(v), side="right") - 1
+    out = np.clip(out, 0, 0x7E).astype(np.uint8)
+    return out | np.where(np.signbit(v), 0x80, 0x00).astype(np.uint8)
+
+
+def _enc_no_saturation(v):
+    # overflow lands on the NaN code instead of +-448
+    out = oracle.encode_e4m3(v)
+    big = np.abs(np.asarray(v, dtype=np.float64)) > 448.0
+    out[big] = out[big] | 0x7F
+    return out
+
+
+def test_oracle_encoder_passes_its_pins():
+    assert check_e4m3_encoder(oracle.encode_e4m3)
+
+
+@pytest.mark.parametrize("bad", [_enc_ties_away, _enc_truncate, _enc_no_saturation])
+def test_mutant_encoder_fails_pin(bad):
+    assert not check_e4m3_encoder(bad)
