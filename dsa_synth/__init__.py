@@ -106,7 +106,9 @@ def quantize_e4m3_rows(x: torch.Tensor):
     rows = x.shape[0]
     flat = x.reshape(rows, -1)
     amax = flat.abs().amax(dim=1)
-    scale = torch.where(amax > 0, amax / E4M3_MAX, torch.ones_like(amax))
+    # a tensor divisor: division by a Python scalar may run as a multiply by
+    # its reciprocal, one ulp away from the IEEE quotient the definition uses
+    scale = torch.where(amax > 0, amax / torch.full_like(amax, E4M3_MAX), torch.ones_like(amax))
     y = (flat / scale[:, None]).clamp_(-E4M3_MAX, E4M3_MAX)
     codes = y.to(torch.float8_e4m3fn).view(torch.uint8).reshape(x.shape)
     return codes, scale.to(torch.float32)

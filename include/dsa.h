@@ -206,6 +206,23 @@ dsa_status_t dsa_sparse_mla_noalloc(const dsa_batch_t* batch, const dsa_mla_t* m
                                     const int32_t* idx, int32_t k, void* out, float* lse,
                                     cudaStream_t stream);
 
+/* Producer step of the indexer inputs: per-group absmax e4m3 quantisation
+ * ("DeepSeek V3.2: How Far Can Open Models Go If You Actually Try?", §3.1:
+ * the indexer runs in FP8; e4m3 codes with one fp32 scale per query token and
+ * per key row).  x holds `groups` groups of `group_elems` consecutive values
+ * (dtype F32 or BF16): a token's H_I x d_I indexer query (group_elems =
+ * 64 * 128) or a key row (group_elems = 128).  For each group:
+ *   scales[g] = amax / 448 in fp32 (1 when amax = 0),
+ *   codes[g * group_elems + i] = e4m3(x / scales[g]), the division in IEEE
+ *   fp32, rounded to nearest even and saturated at +-448.
+ * codes and scales may point into a larger cache at a row offset (appending
+ * new keys to a key cache).  group_elems must be a multiple of 4 in
+ * [4, 16384]; x must be 16-byte aligned, codes and scales 4-byte aligned,
+ * else DSA_ERROR_INVALID_VALUE.  groups = 0 is a no-op.  Caller-owned
+ * device memory; enqueued on `stream`. */
+dsa_status_t dsa_quantize_e4m3(const void* x, dsa_dtype_t x_dtype, int64_t groups, int32_t group_elems,
+                               uint8_t* codes, float* scales, cudaStream_t stream);
+
 /* The whole forward pass: steps 1-3 for every query row, processed in query
  * chunks sized to ws_bytes.  out/lse as dsa_sparse_mla; idx_out (nullable)
  * [total_q, k] receives the selected positions as dsa_topk writes them. */

@@ -77,6 +77,7 @@ _sig = {
     "dsa_workspace_size": (ctypes.c_int, [_P, _P, _P, ctypes.c_int32, ctypes.POINTER(ctypes.c_size_t),
                                           ctypes.POINTER(ctypes.c_size_t)]),
     "dsa_index_scores": (ctypes.c_int, [_P, _P, _P, ctypes.c_int64, _P]),
+    "dsa_quantize_e4m3": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_int64, ctypes.c_int32, _P, _P, _P]),
     "dsa_topk": (ctypes.c_int, [_P, _P, ctypes.c_int64, ctypes.c_int32, _P, _P, _P]),
     "dsa_sparse_mla": (ctypes.c_int, [_P, _P, _P, ctypes.c_int32, _P, _P, _P, ctypes.c_size_t, _P]),
     "dsa_sparse_mla_noalloc": (ctypes.c_int, [_P, _P, _P, ctypes.c_int32, _P, _P, _P]),
@@ -252,6 +253,21 @@ class Trace:
             self.events[n - 1].synchronize()
         return [(KERNEL_NAMES.get(int(self._ids[i]), "?"), self.events[i].elapsed_time(self.events[i + 1]))
                 for i in range(n - 1)]
+
+
+def quantize_e4m3(x, codes, scales, group_elems: int, stream=None):
+    """Per-group absmax e4m3 quantisation (dsa_quantize_e4m3): x (float32 or
+    bfloat16 CUDA tensor) is read as groups of `group_elems` consecutive
+    values; codes (uint8, x.numel() elements) and scales (float32, one per
+    group) may be views into a larger cache."""
+    import torch
+    dt = {torch.float32: DTYPE_F32, torch.bfloat16: DTYPE_BF16}.get(x.dtype)
+    if dt is None:
+        raise ValueError("quantize_e4m3: x must be float32 or bfloat16")
+    if x.numel() % group_elems:
+        raise ValueError("quantize_e4m3: x.numel() must be a multiple of group_elems")
+    _check(lib().dsa_quantize_e4m3(_ptr(x), dt, x.numel() // group_elems, int(group_elems), _ptr(codes),
+                                   _ptr(scales), _stream(stream)), "dsa_quantize_e4m3")
 
 
 def forward(batch: Batch, indexer: Indexer, mla: Mla, k: int, out, lse=None, idx_out=None, ws=None,

@@ -18,6 +18,7 @@
 #include "common.cuh"
 #include "indexer_tc.cuh"
 #include "mla_tc.cuh"
+#include "quant.cuh"
 #include "ptx.cuh"
 #include "simt.cuh"
 #include "topk.cuh"
@@ -558,6 +559,33 @@ dsa_status_t dsa_sparse_mla_noalloc(const dsa_batch_t* batch, const dsa_mla_t* m
   Tracer tr{nullptr, stream};
   return launch_sparse_mla(*dev, batch, mla, idx, k, out, lse, scratch, kStaticScratchBytes, 0,
                            batch->total_q, stream, tr);
+}
+
+dsa_status_t dsa_quantize_e4m3(const void* x, dsa_dtype_t x_dtype, int64_t groups, int32_t group_elems,
+                               uint8_t* codes, float* scales, cudaStream_t stream) {
+  if (groups < 0) return fail(DSA_ERROR_INVALID_VALUE, "groups must be >= 0");
+  if (group_elems < 4 || group_elems > dsa::quant::kMaxGroup || group_elems % 4 != 0)
+    return fail(DSA_ERROR_INVALID_VALUE, "group_elems must be a multiple of 4 in [4, %d]", dsa::quant::kMaxGroup);
+  if (x_dtype != DSA_DTYPE_F32 && x_dtype != DSA_DTYPE_BF16)
+    return fail(DSA_ERROR_NOT_SUPPORTED, "quantize: x dtype must be F32 or BF16");
+  if (groups == 0) return DSA_SUCCESS;
+  if (!x || !codes || !scales) return fail(DSA_ERROR_INVALID_VALUE, "quantize: x, codes and scales are required");
+  if (!aligned16(x) || (reinterpret_cast<uintptr_t>(codes) & 3u) || (reinterpret_cast<uintptr_t>(scales) & 3u))
+    return fail(DSA_ERROR_INVALID_VALUE, "quantize: x must be 16-byte aligned, codes and scales 4-byte aligned");
+  if (groups > (int64_t(1) << 31) - 1) return fail(DSA_ERROR_NOT_SUPPORTED, "quantize: too many groups");
+  DeviceInfo* dev;
+  DSA_TRY(device_info(&dev));
+  const bool bf16 = x_dtype == DSA_DTYPE_BF16;
+  if (group_elems <= dsa::quant::kWarpGroupMax) {
+    const int64_t per_cta = dsa::quant::kThreads / 32;
+    const int64_t ctas = (groups + per_cta - 1) / per_cta;
+    dsa::quant::quantize_warp_kernel<<<static_cast<unsigned>(ctas), dsa::quant::kThreads, 0, stream>>>(
+        x, bf16, groups, group_elems, codes, scales);
+  } else {
+    dsa::quant::quantize_cta_kernel<<<static_cast<unsigned>(groups), dsa::quant::kThreads, 0, stream>>>(
+        x, bf16, group_elems, codes, scales);
+  }
+  return check_launch("quantize_e4m3");
 }
 
 dsa_status_t dsa_forward_traced(const dsa_batch_t* batch, const dsa_indexer_t* indexer, const dsa_mla_t* mla,
