@@ -51,6 +51,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=25.0, help="target oracle time per sample")
     ap.add_argument("--decode-steps", type=int, default=10,
                     help="timed steps of the ragged 128K decode measurement (0 = skip)")
+    ap.add_argument("--dense-steps", type=int, default=1,
+                    help="timed calls of dense MLA over the same prefill, for the sparse/dense ratio (0 = skip)")
     return ap.parse_args()
 
 
@@ -324,6 +326,10 @@ def main():
     if not a.no_e2e:
         e2e = measure_e2e(a, wl, dsa, b, ix, m, out, lse, ws, stream, world, dev)
 
+    dense = None
+    if a.dense_steps > 0:
+        dense = measure_dense(a, dsa, wl, b, m, out, lse, stream, ms_per_step)
+
     decode = None
     if a.decode_steps > 0 and a.workload != "ragged128k":
         del out, lse, ws
@@ -363,6 +369,7 @@ def main():
         "gpu_launches": launches,
         "clocks": clk,
         "decode": decode,
+        "dense_prefill": dense,
     }
     print(json.dumps(line))
 
@@ -446,6 +453,19 @@ def measure_decode(a, dsa, dev, stream):
             per_kernel.setdefault(name, []).append(t)
     if dsa.read_device_errors() != 0:
         raise RuntimeError("device error word set during the decode measurement")
+    # dense baseline: MLA over every cached token of every sequence
+    need = dsa.dense_mla_workspace_size(b, m)
+    dws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev) if need else None
+    dsa.dense_mla(b, m, out, lse, dws, stream=stream)
+    dense_t = []
+    for _ in range(max(3, a.decode_steps // 2)):
+        flush.fill_(1)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        dsa.dense_mla(b, m, out, lse, dws, stream=stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        dense_t.append(e0.elapsed_time(e1))
     peaks, src = load_peaks()
     ms = statistics.median(totals)
     kms = {kname: statistics.median(v) for kname, v in per_kernel.items()}
@@ -459,7 +479,8 @@ def measure_decode(a, dsa, dev, stream):
     mla_ms = kms.get("mla_tc", 0.0) + kms.get("mla_combine", 0.0)
     res = {"workload": wl.name, "tokens_per_step": T, "ms_per_step": ms, "value": T / (ms / 1e3),
            "unit": "tokens/s", "steps": a.decode_steps, "l2": "flushed before every step (512 MiB write)",
-           "kernels_ms_per_step": kms}
+           "kernels_ms_per_step": kms, "dense_mla_ms": statistics.median(dense_t),
+           "dense_mla_over_dsa_step": statistics.median(dense_t) / ms}
     if mla_ms > 0:
         gbs = mla_bytes / (mla_ms / 1e3) / 1e9
         res["mla_hbm"] = {"achieved": gbs, "peak": peaks.get("hbm_gbs"), "unit": "GB/s",
@@ -469,6 +490,28 @@ def measure_decode(a, dsa, dev, stream):
         res["indexer_hbm"] = {"achieved": gbs, "peak": peaks.get("hbm_gbs"), "unit": "GB/s",
                               "frac": gbs / peaks.get("hbm_gbs"), "bytes": idx_bytes}
     return res
+
+
+def measure_dense(a, dsa, wl, b, m, out, lse, stream, dsa_ms):
+    """Dense causal MLA-MQA over every candidate of the same workload (the
+    baseline of the pages' DSA-vs-dense cost claims), against the whole DSA
+    forward step just measured."""
+    import torch
+    need = dsa.dense_mla_workspace_size(b, m)
+    ws = torch.empty(max(need, 16), dtype=torch.uint8, device=out.device) if need else None
+    dsa.dense_mla(b, m, out, lse, ws, stream=stream)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(a.dense_steps):
+        dsa.dense_mla(b, m, out, lse, ws, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / a.dense_steps
+    n = row_candidates(wl.seqlens_q, wl.seqlens_kv).astype(np.float64)
+    flops = 2.0 * wl.n_heads * (wl.d_qk + wl.d_v) * float(n.sum())
+    return {"workload": wl.name, "dense_mla_ms": ms, "dsa_forward_ms": dsa_ms, "dense_over_dsa": ms / dsa_ms,
+            "dense_tflops": flops / (ms / 1e3) / 1e12, "steps": a.dense_steps}
 
 
 def measure_quant(a, dsa, dev, stream):

@@ -206,6 +206,20 @@ dsa_status_t dsa_sparse_mla_noalloc(const dsa_batch_t* batch, const dsa_mla_t* m
                                     const int32_t* idx, int32_t k, void* out, float* lse,
                                     cudaStream_t stream);
 
+/* Dense causal MLA-MQA attention: every query attends to all of its
+ * candidates 0..p (no selection).  This is the baseline sparse selection is
+ * measured against ("DeepSeek V3.2: How Far Can Open Models Go If You
+ * Actually Try?", §3.4: decode at 128K about 2x cheaper than dense MLA; short
+ * prompts run as dense masked attention).  Same layouts and outputs as
+ * dsa_sparse_mla; only the tensor-core instance (128 heads, d_qk 576, d_v 512,
+ * BF16) is supported, else DSA_ERROR_NOT_SUPPORTED.  Batches with fewer rows
+ * than SMs split each row over several CTA pairs; their fp32 partials need
+ * dsa_dense_mla_workspace_size bytes of workspace (0 otherwise), else
+ * DSA_ERROR_INSUFFICIENT_WORKSPACE. */
+dsa_status_t dsa_dense_mla_workspace_size(const dsa_batch_t* batch, const dsa_mla_t* mla, size_t* bytes);
+dsa_status_t dsa_dense_mla(const dsa_batch_t* batch, const dsa_mla_t* mla, void* out, float* lse, void* ws,
+                           size_t ws_bytes, cudaStream_t stream);
+
 /* Producer step of the indexer inputs: per-group absmax e4m3 quantisation
  * ("DeepSeek V3.2: How Far Can Open Models Go If You Actually Try?", §3.1:
  * the indexer runs in FP8; e4m3 codes with one fp32 scale per query token and

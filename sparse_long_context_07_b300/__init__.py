@@ -77,6 +77,8 @@ _sig = {
     "dsa_workspace_size": (ctypes.c_int, [_P, _P, _P, ctypes.c_int32, ctypes.POINTER(ctypes.c_size_t),
                                           ctypes.POINTER(ctypes.c_size_t)]),
     "dsa_index_scores": (ctypes.c_int, [_P, _P, _P, ctypes.c_int64, _P]),
+    "dsa_dense_mla_workspace_size": (ctypes.c_int, [_P, _P, ctypes.POINTER(ctypes.c_size_t)]),
+    "dsa_dense_mla": (ctypes.c_int, [_P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "dsa_quantize_e4m3": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_int64, ctypes.c_int32, _P, _P, _P]),
     "dsa_topk": (ctypes.c_int, [_P, _P, ctypes.c_int64, ctypes.c_int32, _P, _P, _P]),
     "dsa_sparse_mla": (ctypes.c_int, [_P, _P, _P, ctypes.c_int32, _P, _P, _P, ctypes.c_size_t, _P]),
@@ -253,6 +255,21 @@ class Trace:
             self.events[n - 1].synchronize()
         return [(KERNEL_NAMES.get(int(self._ids[i]), "?"), self.events[i].elapsed_time(self.events[i + 1]))
                 for i in range(n - 1)]
+
+
+def dense_mla_workspace_size(batch: Batch, mla: Mla) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().dsa_dense_mla_workspace_size(_ref(batch), _ref(mla), ctypes.byref(n)),
+           "dsa_dense_mla_workspace_size")
+    return int(n.value)
+
+
+def dense_mla(batch: Batch, mla: Mla, out, lse=None, ws=None, stream=None):
+    """Dense causal MLA-MQA attention over every candidate (dsa_dense_mla): the
+    baseline for the sparse path."""
+    nbytes = 0 if ws is None else ws.numel() * ws.element_size()
+    _check(lib().dsa_dense_mla(_ref(batch), _ref(mla), _ptr(out), _ptr(lse), _ptr(ws), nbytes, _stream(stream)),
+           "dsa_dense_mla")
 
 
 def quantize_e4m3(x, codes, scales, group_elems: int, stream=None):

@@ -320,13 +320,36 @@ MlaPlan plan_mla(int sms, int64_t rows, int32_t k, size_t ws_cap = SIZE_MAX) {
   }
 }
 
+// Dense mode: the longest row sets the tile count.  With fewer rows than SMs
+// the rows are also split so that no unit exceeds kDenseTilesPerUnit tiles,
+// which keeps rows of very different lengths from serialising on a few SMs.
+constexpr int kDenseTilesPerUnit = 256;
+MlaPlan plan_dense_mla(int sms, int64_t rows, int32_t max_n, size_t ws_cap = SIZE_MAX) {
+  const int tiles = (max_n + dsa::mla_tc::kRows - 1) / dsa::mla_tc::kRows;
+  const int64_t units_wanted = std::max(1, sms / 2);
+  int want = 1;
+  if (2 * rows < units_wanted) want = static_cast<int>((units_wanted + rows - 1) / rows);
+  if (rows < sms) want = std::max(want, (tiles + kDenseTilesPerUnit - 1) / kDenseTilesPerUnit);
+  want = std::max(1, std::min(want, tiles));
+  for (;; --want) {
+    MlaPlan p;
+    p.tiles_per_split = (tiles + want - 1) / want;
+    p.nsplit = (tiles + p.tiles_per_split - 1) / p.tiles_per_split;
+    if (p.nsplit > 1)
+      p.ws_bytes = static_cast<size_t>(rows) * p.nsplit * dsa::mla_tc::kHeads * (dsa::mla_tc::kDv + 1) * 4 + 256;
+    if (p.ws_bytes <= ws_cap || want <= 1) return p;
+  }
+}
+
 dsa_status_t launch_sparse_mla(const DeviceInfo& dev, const dsa_batch_t* b, const dsa_mla_t* m,
                                const int32_t* idx, int32_t k, void* out, float* lse, void* ws,
-                               size_t ws_bytes, int64_t r0, int64_t r1, cudaStream_t s, Tracer& tr) {
+                               size_t ws_bytes, int64_t r0, int64_t r1, cudaStream_t s, Tracer& tr,
+                               bool dense = false) {
   const int64_t rows = r1 - r0;
   if (rows <= 0) return DSA_SUCCESS;
   if (mla_is_tc(m)) {
-    const MlaPlan plan = plan_mla(dev.sms, rows, k, ws ? ws_bytes : 0);
+    const MlaPlan plan = dense ? plan_dense_mla(dev.sms, rows, k, ws ? ws_bytes : 0)
+                               : plan_mla(dev.sms, rows, k, ws ? ws_bytes : 0);
     if (plan.ws_bytes > ws_bytes || (plan.ws_bytes > 0 && !ws))
       return fail(DSA_ERROR_INSUFFICIENT_WORKSPACE, "sparse MLA needs %zu bytes of workspace, got %zu",
                   plan.ws_bytes, ws_bytes);
@@ -340,6 +363,7 @@ dsa_status_t launch_sparse_mla(const DeviceInfo& dev, const dsa_batch_t* b, cons
     P.kv = static_cast<const __nv_bfloat16*>(m->kv);
     P.idx = idx;
     P.k = k;
+    P.dense = dense ? 1 : 0;
     P.c_log2 = m->scale * 1.4426950408889634f;
     P.cu_q = b->cu_seqlens_q;
     P.cu_kv = b->cu_seqlens_kv;
@@ -537,6 +561,31 @@ dsa_status_t dsa_sparse_mla(const dsa_batch_t* batch, const dsa_mla_t* mla, cons
   return launch_sparse_mla(*dev, batch, mla, idx, k, out, lse, ws, ws_bytes, 0, batch->total_q, stream, tr);
 }
 
+dsa_status_t dsa_dense_mla_workspace_size(const dsa_batch_t* batch, const dsa_mla_t* mla, size_t* bytes) {
+  DSA_TRY(check_batch(batch));
+  DSA_TRY(check_mla(mla, batch));
+  if (!mla_is_tc(mla)) return fail(DSA_ERROR_NOT_SUPPORTED, "dense MLA needs 128 heads, d_qk 576, d_v 512, BF16");
+  size_t need = 0;
+  if (batch->total_q > 0) need = plan_dense_mla(sms_for_sizing(), batch->total_q, std::max(1, batch->max_seqlen_kv)).ws_bytes;
+  if (bytes) *bytes = need;
+  return DSA_SUCCESS;
+}
+
+dsa_status_t dsa_dense_mla(const dsa_batch_t* batch, const dsa_mla_t* mla, void* out, float* lse, void* ws,
+                           size_t ws_bytes, cudaStream_t stream) {
+  DSA_TRY(check_batch(batch));
+  DSA_TRY(check_mla(mla, batch));
+  if (!mla_is_tc(mla)) return fail(DSA_ERROR_NOT_SUPPORTED, "dense MLA needs 128 heads, d_qk 576, d_v 512, BF16");
+  if (batch->total_q == 0) return DSA_SUCCESS;
+  if (!out || !aligned16(out) || (lse && !aligned16(lse)))
+    return fail(DSA_ERROR_INVALID_VALUE, "out must be non-NULL; out and lse 16-byte aligned");
+  DeviceInfo* dev;
+  DSA_TRY(device_info(&dev));
+  Tracer tr{nullptr, stream};
+  return launch_sparse_mla(*dev, batch, mla, nullptr, std::max(1, batch->max_seqlen_kv), out, lse, ws, ws_bytes, 0,
+                           batch->total_q, stream, tr, true);
+}
+
 dsa_status_t dsa_sparse_mla_noalloc(const dsa_batch_t* batch, const dsa_mla_t* mla, const int32_t* idx,
                                     int32_t k, void* out, float* lse, cudaStream_t stream) {
   DSA_TRY(check_batch(batch));
@@ -576,15 +625,15 @@ dsa_status_t dsa_quantize_e4m3(const void* x, dsa_dtype_t x_dtype, int64_t group
   DeviceInfo* dev;
   DSA_TRY(device_info(&dev));
   const bool bf16 = x_dtype == DSA_DTYPE_BF16;
-  if (group_elems <= dsa::quant::kWarpGroupMax) {
-    const int64_t per_cta = dsa::quant::kThreads / 32;
-    const int64_t ctas = (groups + per_cta - 1) / per_cta;
+  const int64_t per_cta = dsa::quant::kThreads / 32;   // one warp per group
+  const int64_t ctas = (groups + per_cta - 1) / per_cta;
+  if (ctas > 2147483647ll) return fail(DSA_ERROR_NOT_SUPPORTED, "quantize: too many groups");
+  if (group_elems <= dsa::quant::kWarpGroupMax)
     dsa::quant::quantize_warp_kernel<<<static_cast<unsigned>(ctas), dsa::quant::kThreads, 0, stream>>>(
         x, bf16, groups, group_elems, codes, scales);
-  } else {
-    dsa::quant::quantize_cta_kernel<<<static_cast<unsigned>(groups), dsa::quant::kThreads, 0, stream>>>(
-        x, bf16, group_elems, codes, scales);
-  }
+  else
+    dsa::quant::quantize_stream_kernel<<<static_cast<unsigned>(ctas), dsa::quant::kThreads, 0, stream>>>(
+        x, bf16, groups, group_elems, codes, scales);
   return check_launch("quantize_e4m3");
 }
 

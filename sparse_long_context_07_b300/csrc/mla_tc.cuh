@@ -40,6 +40,10 @@
 //
 // Split-KV (decode): a CTA may take a contiguous range of tiles of a token; it
 // then writes fp32 (O / l, lse) partials merged by combine_kernel.
+//
+// Dense mode (the baseline that sparse selection is measured against): no
+// index list, every candidate 0..p of the row is attended, i.e. causal
+// MLA-MQA attention over the whole context.
 #pragma once
 
 #include <cstdint>
@@ -88,8 +92,9 @@ constexpr int kSmemBytes = kOffMisc + 16 + 1024;
 struct Params {
   const __nv_bfloat16* q;    // [total_q, 128, 576]
   const __nv_bfloat16* kv;   // [total_kv, 576]
-  const int32_t* idx;        // [rows of this launch, k], relative to row0
-  int k;
+  const int32_t* idx;        // [rows of this launch, k], relative to row0 (unused when dense)
+  int k;                     // selected entries per row (dense: the longest row's candidates)
+  int dense;                 // 1: attend over every candidate 0..p (no index list)
   float c_log2;              // scale * log2(e)
   const int32_t* cu_q;
   const int32_t* cu_kv;
@@ -153,12 +158,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t row = P.row0 + rrel;
   const RowGeom geo = row_geom(P.cu_q, P.cu_kv, P.num_seqs, row);
   const int n = geo.p + 1;
-  const int tiles_total = (P.k + kRows - 1) / kRows;
+  // dense: a row's own candidates bound its tiles
+  const int tiles_total = (((P.dense && n < P.k) ? n : P.k) + kRows - 1) / kRows;
   const int t_begin = split * P.tiles_per_split;
   int t_end = t_begin + P.tiles_per_split;
   if (t_end > tiles_total) t_end = tiles_total;
   const int nt = t_end > t_begin ? t_end - t_begin : 0;
-  const int32_t* __restrict__ idx_row = P.idx + rrel * static_cast<int64_t>(P.k);
+  const int32_t* __restrict__ idx_row = P.dense ? nullptr : P.idx + rrel * static_cast<int64_t>(P.k);
+  // selected position of entry e of this row (-1: none)
+  auto sel_at = [&](int e) -> int {
+    if (P.dense) return e < n ? e : -1;
+    return e < P.k ? __ldg(idx_row + e) : -1;
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -196,7 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int i = gt >> 3, t8 = gt & 7;
     auto load_idx = [&](int j) -> int {
       const int e = (t_begin + j) * kRows + i;
-      return (j < nt && e < P.k) ? __ldg(idx_row + e) : -1;
+      return j < nt ? sel_at(e) : -1;
     };
     int s_cur = load_idx(0), s_next = load_idx(1);
     for (int j = 0; j < nt; ++j) {
@@ -310,7 +321,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float m_use = -INFINITY, l = 0.f;
     auto load_sel = [&](int j) -> int {
       const int e = (t_begin + j) * kRows + lane;
-      return (j < nt && e < P.k) ? __ldg(idx_row + e) : -1;
+      return j < nt ? sel_at(e) : -1;
     };
     int sel_next = load_sel(0);
     for (int j = 0; j < nt; ++j) {

@@ -9,9 +9,9 @@
 // and saturating at +-448 (cvt.rn.satfinite).  The codes and scales can be
 // written straight into a cache at a row offset (append).
 //
-// Groups of at most 1024 values take one warp each (8 per 256-thread CTA);
-// larger groups (up to 16384) take a whole CTA.  Every thread keeps its
-// values in registers between the max and the conversion.
+// Groups of at most 1024 values take one warp each (8 per 256-thread CTA) and
+// stay in registers between the max and the conversion; larger groups (up to
+// 16384) take one warp each in two streaming passes.
 #pragma once
 
 #include <cstdint>
@@ -21,9 +21,8 @@ namespace dsa {
 namespace quant {
 
 constexpr int kThreads = 256;
-constexpr int kMaxPerThread = 64;          // values a thread holds
 constexpr int kWarpGroupMax = 32 * 32;     // largest group handled by one warp
-constexpr int kMaxGroup = kThreads * kMaxPerThread;
+constexpr int kMaxGroup = 16384;
 
 // Four consecutive inputs as fp32 (bf16 widens exactly).
 __device__ __forceinline__ float4 load4(const void* x, int64_t i, bool bf16) {
@@ -81,37 +80,47 @@ __global__ void __launch_bounds__(kThreads) quantize_warp_kernel(const void* __r
   if (lane == 0) scales[g] = scale;
 }
 
-// One CTA per group (group_elems <= 16384, multiple of 4).
-__global__ void __launch_bounds__(kThreads) quantize_cta_kernel(const void* __restrict__ x, bool bf16,
-                                                                 int group_elems, uint8_t* __restrict__ codes,
-                                                                 float* __restrict__ scales) {
-  __shared__ float warp_max[kThreads / 32];
-  const int tid = threadIdx.x;
-  const int64_t g = blockIdx.x;
+// Groups larger than a warp's register share (up to 16384 values): one warp
+// per group in two streaming passes, the absmax pass from HBM and the
+// encoding pass re-reading the group (16 KB at most, still in L2), with eight
+// loads in flight per lane in each pass.
+__global__ void __launch_bounds__(kThreads) quantize_stream_kernel(const void* __restrict__ x, bool bf16,
+                                                                    int64_t groups, int group_elems,
+                                                                    uint8_t* __restrict__ codes,
+                                                                    float* __restrict__ scales) {
+  const int lane = threadIdx.x & 31;
+  const int64_t g = static_cast<int64_t>(blockIdx.x) * (kThreads / 32) + (threadIdx.x >> 5);
+  if (g >= groups) return;
   const int nvec = group_elems / 4;
   const int64_t base = g * group_elems;
-  float4 v[kMaxPerThread / 4];
   float amax = 0.f;
+  for (int q0 = 0; q0 < nvec; q0 += 32 * 8) {
+    float4 v[8];
 #pragma unroll
-  for (int r = 0; r < kMaxPerThread / 4; ++r) {
-    const int q = tid + kThreads * r;
-    v[r] = q < nvec ? load4(x, base + 4 * q, bf16) : make_float4(0.f, 0.f, 0.f, 0.f);
-    amax = fmaxf(amax, absmax4(v[r]));
+    for (int u = 0; u < 8; ++u) {
+      const int q = q0 + lane + 32 * u;
+      v[u] = q < nvec ? load4(x, base + 4 * q, bf16) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) amax = fmaxf(amax, absmax4(v[u]));
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-  if ((tid & 31) == 0) warp_max[tid >> 5] = amax;
-  __syncthreads();
-  amax = warp_max[0];
-#pragma unroll
-  for (int w = 1; w < kThreads / 32; ++w) amax = fmaxf(amax, warp_max[w]);
   const float scale = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+  for (int q0 = 0; q0 < nvec; q0 += 32 * 8) {
+    float4 v[8];
 #pragma unroll
-  for (int r = 0; r < kMaxPerThread / 4; ++r) {
-    const int q = tid + kThreads * r;
-    if (q < nvec) reinterpret_cast<uint32_t*>(codes + base)[q] = encode4(v[r], scale);
+    for (int u = 0; u < 8; ++u) {
+      const int q = q0 + lane + 32 * u;
+      v[u] = q < nvec ? load4(x, base + 4 * q, bf16) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int q = q0 + lane + 32 * u;
+      if (q < nvec) reinterpret_cast<uint32_t*>(codes + base)[q] = encode4(v[u], scale);
+    }
   }
-  if (tid == 0) scales[g] = scale;
+  if (lane == 0) scales[g] = scale;
 }
 
 }  // namespace quant
