@@ -323,7 +323,7 @@ MlaPlan plan_mla(int sms, int64_t rows, int32_t k, size_t ws_cap = SIZE_MAX) {
 // Dense mode: the longest row sets the tile count.  With fewer rows than SMs
 // the rows are also split so that no unit exceeds kDenseTilesPerUnit tiles,
 // which keeps rows of very different lengths from serialising on a few SMs.
-constexpr int kDenseTilesPerUnit = 256;
+constexpr int kDenseTilesPerUnit = 128;
 MlaPlan plan_dense_mla(int sms, int64_t rows, int32_t max_n, size_t ws_cap = SIZE_MAX) {
   const int tiles = (max_n + dsa::mla_tc::kRows - 1) / dsa::mla_tc::kRows;
   const int64_t units_wanted = std::max(1, sms / 2);
