@@ -96,7 +96,9 @@ dsa_status_t device_info(DeviceInfo** out) {
         cudaFuncSetAttribute(dsa::mla_tc::mla_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              dsa::mla_tc::kSmemBytes) != cudaSuccess ||
         cudaFuncSetAttribute(dsa::topk::topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             dsa::topk::kSmemBytes) != cudaSuccess)
+                             dsa::topk::kSmemBytes) != cudaSuccess ||
+        cudaFuncSetAttribute(dsa::topk::topk_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             dsa::topk::kCSmemBytes) != cudaSuccess)
       return fail(DSA_ERROR_LAUNCH, "cudaFuncSetAttribute failed: %s",
                   cudaGetErrorString(cudaGetLastError()));
     d.attrs_set = true;
@@ -278,8 +280,19 @@ dsa_status_t launch_index_scores(const DeviceInfo& dev, const dsa_batch_t* b, co
   return DSA_SUCCESS;
 }
 
-dsa_status_t launch_topk(const dsa_batch_t* b, const float* scores, int64_t ld, int32_t k, int32_t* idx,
-                         float* vals, int64_t r0, int64_t r1, cudaStream_t s, Tracer& tr) {
+// A few rows (a decode batch) cannot fill the device one CTA per row: each
+// row then gets a cluster of CTAs, each taking a slice of the row.
+dsa_status_t launch_topk(const DeviceInfo& dev, const dsa_batch_t* b, const float* scores, int64_t ld,
+                         int32_t k, int32_t* idx, float* vals, int64_t r0, int64_t r1, cudaStream_t s,
+                         Tracer& tr) {
+  if (r1 > r0 && (r1 - r0) * dsa::topk::kCluster <= 4 * static_cast<int64_t>(dev.sms)) {
+    dsa::topk::topk_cluster_kernel<<<static_cast<unsigned>((r1 - r0) * dsa::topk::kCluster),
+                                     dsa::topk::kCThreads, dsa::topk::kCSmemBytes, s>>>(
+        scores, ld, k, idx, vals, b->cu_seqlens_q, b->cu_seqlens_kv, b->num_seqs, r0);
+    DSA_TRY(check_launch("topk_cluster"));
+    tr.after(DSA_KERNEL_TOPK);
+    return DSA_SUCCESS;
+  }
   for (int64_t c = r0; c < r1; c += 2147483647ll) {
     const int64_t e = std::min<int64_t>(r1, c + 2147483647ll);
     dsa::topk::topk_kernel<<<static_cast<unsigned>(e - c), dsa::topk::kThreads, dsa::topk::kSmemBytes, s>>>(
@@ -544,7 +557,7 @@ dsa_status_t dsa_topk(const dsa_batch_t* batch, const float* scores, int64_t ld_
   DeviceInfo* dev;
   DSA_TRY(device_info(&dev));
   Tracer tr{nullptr, stream};
-  return launch_topk(batch, scores, ld_scores, k, idx, vals, 0, batch->total_q, stream, tr);
+  return launch_topk(*dev, batch, scores, ld_scores, k, idx, vals, 0, batch->total_q, stream, tr);
 }
 
 dsa_status_t dsa_sparse_mla(const dsa_batch_t* batch, const dsa_mla_t* mla, const int32_t* idx, int32_t k,
@@ -675,7 +688,7 @@ dsa_status_t dsa_forward_traced(const dsa_batch_t* batch, const dsa_indexer_t* i
     const int64_t r1 = std::min<int64_t>(batch->total_q, r0 + plan.chunk);
     int32_t* idx = idx_out ? idx_out + r0 * k : idx_ws;
     DSA_TRY(launch_index_scores(*dev, batch, indexer, scores, plan.ld, r0, r1, stream, tr));
-    DSA_TRY(launch_topk(batch, scores, plan.ld, k, idx, nullptr, r0, r1, stream, tr));
+    DSA_TRY(launch_topk(*dev, batch, scores, plan.ld, k, idx, nullptr, r0, r1, stream, tr));
     DSA_TRY(launch_sparse_mla(*dev, batch, mla, idx, k,
                               static_cast<char*>(out) + r0 * mla->n_heads * mla->d_v * static_cast<int64_t>(esz),
                               lse ? lse + r0 * mla->n_heads : nullptr, mla_ws, plan.mla_bytes, r0, r1, stream, tr));

@@ -5,7 +5,8 @@
 // the System Modules of "DeepSeek-V3.2: Pushing the Frontier of Open Large
 // Language Models").  Ties go to the lower position; -0.0 == +0.0.
 //
-// One CTA per row.  Scores map to order-preserving 32-bit keys.
+// topk_kernel: one CTA per row (topk_cluster_kernel below serves batches of
+// few rows).  Scores map to order-preserving 32-bit keys.
 //   pass 1 (row read once): histogram of the top 11 key bits; the bin b* that
 //            holds the k-th largest key and the count above it follow from a
 //            block scan.
@@ -25,6 +26,7 @@
 #include <cstdint>
 
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace dsa {
 namespace topk {
@@ -319,6 +321,252 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(
       const int b = __ffs(bits) - 1;
       bits &= bits - 1u;
       const int i = 32 * w + b;
+      if (pos < static_cast<uint32_t>(k)) {
+        out_idx[pos] = i;
+        if (out_val) out_val[pos] = __ldg(row + i);
+      }
+      ++pos;
+    }
+  }
+}
+
+// ----------------------------------------------------------------------------
+// Few long rows (decode): a cluster of kCluster CTAs per row.
+//
+// CTA c of a row's cluster owns the contiguous slice [c S, c S + S) of the
+// candidates (S a multiple of 32).  It reads its slice once and keeps the
+// order keys in shared memory (slices up to kSliceCap; longer ones are read
+// from global memory in every pass).  The exact k-th largest key T follows
+// from three radix passes (digits of 11, 11 and 10 bits); in each pass every
+// CTA histograms its slice, CTA c adds bins [256 c, 256 c + 256) of all the
+// CTAs' histograms through distributed shared memory and writes the sums
+// into every CTA's copy of the row histogram, so each CTA finds the same
+// digit.  Then each CTA marks its keys above T and equal to T in bitmaps, the
+// CTAs swap their counts, and CTA c takes the ties left after the CTAs before
+// it (the lowest positions win) and writes its selection at the offset the
+// CTAs before it fill.  Same result as topk_kernel, bit for bit.
+// ----------------------------------------------------------------------------
+constexpr int kCluster = 8;
+constexpr int kCThreads = 256;
+constexpr int kSliceCap = 16384;
+static_assert(kBins == kCluster * kCThreads, "one histogram bin per thread in the cluster reduction");
+
+struct CSmem {
+  uint32_t keys[kSliceCap];
+  uint32_t hist[kBins];          // this CTA's histogram of the pass
+  uint32_t ghist[kBins];         // the row's histogram of the pass
+  uint32_t sel[kSliceCap / 32];
+  uint32_t tie[kSliceCap / 32];
+  uint32_t warp_sums[32];
+  uint32_t cnt[2 * kCluster];    // (selected, tied) keys of every CTA of the cluster
+  uint32_t s_digit, s_above;
+};
+constexpr int kCSmemBytes = static_cast<int>(sizeof(CSmem));
+
+__device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+// The digit holding the kr-th largest key of hist (nbins <= 2048 bins;
+// thread t owns bins [8t, 8t + 8)) and the number of keys in higher bins.
+__device__ __forceinline__ void find_digit_c(const uint32_t* hist, int nbins, uint32_t kr, CSmem& sm) {
+  const int tid = threadIdx.x;
+  uint32_t c[8], s = 0;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    c[q] = (8 * tid + q < nbins) ? hist[8 * tid + q] : 0u;
+    s += c[q];
+  }
+  uint32_t total;
+  const uint32_t incl = block_inclusive_scan<kCThreads>(s, sm.warp_sums, total);
+  const uint32_t above = total - incl;
+  if (above < kr && above + s >= kr) {
+    uint32_t a = above;
+#pragma unroll
+    for (int q = 7; q >= 0; --q) {
+      if (a + c[q] >= kr) { sm.s_digit = 8 * tid + q; sm.s_above = a; break; }
+      a += c[q];
+    }
+  }
+  __syncthreads();
+}
+
+__global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kCThreads) topk_cluster_kernel(
+    const float* __restrict__ scores, int64_t ld, int k, int32_t* __restrict__ idx,
+    float* __restrict__ vals, const int32_t* __restrict__ cu_q, const int32_t* __restrict__ cu_kv,
+    int num_seqs, int64_t row0) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  CSmem& sm = *reinterpret_cast<CSmem*>(smem_raw);
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int c = static_cast<int>(cluster_ctarank());
+  const int64_t rl = blockIdx.x / kCluster;   // row within this launch
+  const int64_t r = row0 + rl;
+  const RowGeom g = row_geom(cu_q, cu_kv, num_seqs, r);
+  const int n = g.p + 1;
+  const float* __restrict__ row = scores + rl * ld;
+  int32_t* __restrict__ out_idx = idx + rl * static_cast<int64_t>(k);
+  float* __restrict__ out_val = vals ? vals + rl * static_cast<int64_t>(k) : nullptr;
+
+  if (n <= k) {  // every candidate is selected (uniform per cluster: no barrier is reached)
+    for (int i = c * kCThreads + tid; i < k; i += kCluster * kCThreads) {
+      out_idx[i] = i < n ? i : -1;
+      if (out_val) out_val[i] = i < n ? row[i] : -__int_as_float(0x7f800000);
+    }
+    return;
+  }
+
+  const int S = ((n + 32 * kCluster - 1) / (32 * kCluster)) * 32;
+  const int lo = c * S;
+  const int len = max(0, min(n, lo + S) - lo);
+  const bool cached = S <= kSliceCap;   // uniform per cluster
+  const float* __restrict__ slice = row + lo;
+  if (cached) {
+    const int n4 = len >> 2;
+    const float4* __restrict__ s4 = reinterpret_cast<const float4*>(slice);
+    auto put = [&](int i, const float4& v) {
+      sm.keys[4 * i] = order_key(v.x);
+      sm.keys[4 * i + 1] = order_key(v.y);
+      sm.keys[4 * i + 2] = order_key(v.z);
+      sm.keys[4 * i + 3] = order_key(v.w);
+    };
+    // eight 16-byte loads in flight per thread
+    int i = tid;
+    for (; i + 7 * kCThreads < n4; i += 8 * kCThreads) {
+      float4 v[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) v[q] = __ldg(s4 + i + q * kCThreads);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) put(i + q * kCThreads, v[q]);
+    }
+    for (; i < n4; i += kCThreads) put(i, __ldg(s4 + i));
+    for (int t = 4 * n4 + tid; t < len; t += kCThreads) sm.keys[t] = order_key(__ldg(slice + t));
+  }
+  auto key_at = [&](int i) -> uint32_t { return cached ? sm.keys[i] : order_key(__ldg(slice + i)); };
+
+  const uint32_t hist_base = smem_u32(sm.hist), ghist_base = smem_u32(sm.ghist);
+  uint32_t prefix = 0, pmask = 0, kr = static_cast<uint32_t>(k);
+#pragma unroll 1
+  for (int pass = 0; pass < 3; ++pass) {
+    const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
+    const uint32_t dmask = pass == 2 ? 0x3FFu : 0x7FFu;
+    for (int i = tid; i < kBins; i += kCThreads) sm.hist[i] = 0u;
+    __syncthreads();
+    for (int i = tid; i < len; i += kCThreads) {
+      const uint32_t key = key_at(i);
+      if ((key & pmask) == prefix) atomicAdd(&sm.hist[(key >> shift) & dmask], 1u);
+    }
+    __syncthreads();
+    cluster_sync();   // every CTA's histogram is complete
+    {
+      const int b = kCThreads * c + tid;   // this thread's bin of the row histogram
+      uint32_t v = 0;
+#pragma unroll
+      for (int q = 0; q < kCluster; ++q) v += ld_cluster_u32(mapa_shared(hist_base + 4u * b, q));
+#pragma unroll
+      for (int q = 0; q < kCluster; ++q) st_cluster_u32(mapa_shared(ghist_base + 4u * b, q), v);
+    }
+    cluster_sync();   // every CTA holds the row histogram; the local ones may be reused
+    find_digit_c(sm.ghist, pass == 2 ? 1024 : kBins, kr, sm);
+    kr -= sm.s_above;
+    prefix |= sm.s_digit << shift;
+    pmask |= dmask << shift;
+    __syncthreads();
+  }
+  const uint32_t T = prefix;   // the k-th largest key; kr keys equal to it are taken
+
+  // ---- bitmaps of the slice: keys above T, keys equal to T (one word per
+  // warp iteration: lane j looks at position 32 w + j)
+  const int nwords = (len + 31) >> 5;
+  uint32_t sel_cnt = 0, tie_cnt = 0;
+  for (int w = warp; w < nwords; w += kCThreads / 32) {
+    const int i = 32 * w + lane;
+    const uint32_t key = i < len ? key_at(i) : 0u;
+    const uint32_t bs = __ballot_sync(0xffffffffu, i < len && key > T);
+    const uint32_t bt = __ballot_sync(0xffffffffu, i < len && key == T);
+    if (lane == 0) {
+      if (cached) {
+        sm.sel[w] = bs;
+        sm.tie[w] = bt;
+      }
+      sel_cnt += __popc(bs);
+      tie_cnt += __popc(bt);
+    }
+  }
+  uint32_t tot_sel, tot_tie;
+  block_inclusive_scan<kCThreads>(sel_cnt, sm.warp_sums, tot_sel);
+  block_inclusive_scan<kCThreads>(tie_cnt, sm.warp_sums, tot_tie);
+  if (tid < kCluster) {
+    const uint32_t base = smem_u32(sm.cnt);
+    st_cluster_u32(mapa_shared(base + 8u * c, tid), tot_sel);
+    st_cluster_u32(mapa_shared(base + 8u * c + 4u, tid), tot_tie);
+  }
+  cluster_sync();   // every CTA holds all counts; no shared memory is read remotely after this
+  // ties go to the lowest positions: the CTAs before this one take theirs first
+  uint32_t ties_before = 0, out_base = 0;
+  for (int q = 0; q < c; ++q) {
+    const uint32_t tq = sm.cnt[2 * q + 1];
+    const uint32_t take_q = ties_before >= kr ? 0u : min(kr - ties_before, tq);
+    out_base += sm.cnt[2 * q] + take_q;
+    ties_before += tq;
+  }
+  const uint32_t kr_here = ties_before >= kr ? 0u : kr - ties_before;   // ties this CTA may take
+
+  // ---- ordered emission of the slice: thread t scans words [wpt t, wpt t + wpt)
+  constexpr int kWpt = kSliceCap / 32 / kCThreads;   // 2 words per thread when cached
+  const int wpt = cached ? kWpt : (nwords + kCThreads - 1) / kCThreads;
+  // slices longer than kSliceCap keep no bitmaps: the words are rebuilt from
+  // the keys below when needed
+  auto words = [&](int w, uint32_t& bs, uint32_t& bt) {
+    if (cached) {
+      bs = sm.sel[w];
+      bt = sm.tie[w];
+    } else {
+      bs = 0u; bt = 0u;
+      for (int j = 0; j < 32; ++j) {
+        const int i = 32 * w + j;
+        if (i < len) {
+          const uint32_t key = key_at(i);
+          bs |= (key > T ? 1u : 0u) << j;
+          bt |= (key == T ? 1u : 0u) << j;
+        }
+      }
+    }
+  };
+  const int w0 = tid * wpt;
+  uint32_t my_sel = 0, my_tie = 0;
+  for (int q = 0; q < wpt; ++q) {
+    if (w0 + q < nwords) {
+      uint32_t bs, bt;
+      words(w0 + q, bs, bt);
+      my_sel += __popc(bs);
+      my_tie += __popc(bt);
+    }
+  }
+  uint32_t tot;
+  const uint32_t tie_before = block_inclusive_scan<kCThreads>(my_tie, sm.warp_sums, tot) - my_tie;
+  uint32_t take = tie_before >= kr_here ? 0u : min(kr_here - tie_before, my_tie);
+  const uint32_t out_cnt = my_sel + take;
+  uint32_t pos = out_base + block_inclusive_scan<kCThreads>(out_cnt, sm.warp_sums, tot) - out_cnt;
+  for (int q = 0; q < wpt; ++q) {
+    const int w = w0 + q;
+    if (w >= nwords) break;
+    uint32_t bits, tb;
+    words(w, bits, tb);
+    while (take > 0u && tb != 0u) {   // the lowest positions of the ties
+      bits |= tb & (0u - tb);
+      tb &= tb - 1u;
+      --take;
+    }
+    while (bits != 0u) {
+      const int b = __ffs(bits) - 1;
+      bits &= bits - 1u;
+      const int i = lo + 32 * w + b;
       if (pos < static_cast<uint32_t>(k)) {
         out_idx[pos] = i;
         if (out_val) out_val[pos] = __ldg(row + i);
