@@ -95,3 +95,29 @@ def test_topk_rows_beyond_the_bitmap_and_boundary_overflow():
     kth = torch.sort(row[:9000], descending=True).values[k - 100]
     row[1000:7000] = kth
     _check(batch, scores, ld, k, range(len(lens)), dict(enumerate(lens)))
+
+
+def test_topk_cluster_and_row_kernels_agree():
+    # a batch of few rows takes a cluster of CTAs per row, a larger batch one
+    # CTA per row; the same rows must come out identical either way
+    props = torch.cuda.get_device_properties(0)
+    few = (4 * props.multi_processor_count) // 8          # largest batch on the cluster path
+    lens = [16384 + 997 * i for i in range(few + 1)]
+    k = 2048
+    ld = ((max(lens) + 3) // 4) * 4
+    for kind in ("normal", "ties"):
+        scores = _scores(len(lens), ld, kind, seed=21)
+        outs = []
+        for rows in (few, few + 1):
+            sub = lens[:rows]
+            batch = dsa.Batch(_cu([1] * rows), _cu(sub), [1] * rows, sub)
+            idx = torch.full((rows, k), -7, dtype=torch.int32, device="cuda")
+            dsa.topk(batch, scores, ld, k, idx)
+            torch.cuda.synchronize()
+            assert dsa.read_device_errors() == 0
+            outs.append(idx[:few].cpu())
+        assert torch.equal(outs[0], outs[1]), kind
+        S = scores.cpu().numpy()
+        for r in (0, few // 2, few - 1):
+            ref = oracle.topk_indices(S[r, :lens[r]].astype(np.float64), k)
+            assert np.array_equal(outs[0][r].numpy(), ref), f"{kind} row {r}"
