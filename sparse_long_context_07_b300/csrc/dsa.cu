@@ -250,9 +250,12 @@ dsa_status_t launch_index_scores(const DeviceInfo& dev, const dsa_batch_t* b, co
     P.group = dsa::idx_tc::kMaxTokens;
     P.fault = g_fault_next.exchange(0);
     if (b->max_seqlen_q == 1) {
-      // decode: one token per sequence; split long key ranges so every SM works
+      // decode: one token per sequence; split long key ranges so every SM
+      // works.  CTAs take items round-robin, so items of about 16 tiles
+      // (16 per SM) keep the last round short; smaller ones cost more in
+      // per-item start-up than they save.
       const int64_t tiles = (b->total_kv + dsa::idx_tc::kKeys - 1) / dsa::idx_tc::kKeys + b->num_seqs;
-      const int64_t target = 4ll * dev.sms;
+      const int64_t target = 16ll * dev.sms;
       P.max_tiles = static_cast<int>(std::max<int64_t>(8, (tiles + target - 1) / target));
     } else {
       P.max_tiles = 1 << 24;
