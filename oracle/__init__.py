@@ -26,3 +26,9 @@ from .dsa_oracle import (  # noqa: F401
     lse_merge,
     forward_rows,
 )
+from .indexer_loss import (  # noqa: F401
+    dense_attention_target_row,
+    kl_to_softmax_row,
+    indexer_scores_backward_row,
+    indexer_warmup_loss,
+)
