@@ -250,6 +250,50 @@ dsa_status_t dsa_forward_traced(const dsa_batch_t* batch, const dsa_indexer_t* i
                                 int32_t* idx_out, void* ws, size_t ws_bytes,
                                 cudaStream_t stream, dsa_trace_t* trace);
 
+/* Host copies of the inputs of dsa_forward_streamed.  Each pointer is the
+ * host-memory counterpart of the device tensor with the same role in
+ * dsa_indexer_t / dsa_mla_t (same shape and dtype); q_scale / k_scale are
+ * NULL exactly when the device ones are.  Page-locked (pinned) host memory
+ * lets the copies overlap the kernels; pageable memory works but serialises
+ * them. */
+typedef struct {
+  const void* idx_q;       /* indexer q        [total_q, n_heads, head_dim] */
+  const float* idx_q_scale;/* indexer q_scale  [total_q] or NULL */
+  const void* idx_k;       /* indexer k        [total_kv, head_dim] */
+  const float* idx_k_scale;/* indexer k_scale  [total_kv] or NULL */
+  const float* idx_w;      /* indexer w        [total_q, n_heads] */
+  const void* mla_q;       /* mla q            [total_q, n_heads, d_qk] */
+  const void* mla_kv;      /* mla kv           [total_kv, d_qk] */
+} dsa_host_inputs_t;
+
+/* dsa_forward for inputs that live in host memory, with the output returned
+ * to host memory.  The pages have no counterpart: this is the serving-side
+ * integration of the same three steps.
+ *
+ * Copies and kernels overlap:
+ *   - the key-side inputs (indexer k, k_scale and the latent cache) are
+ *     copied in full first;
+ *   - the query-side inputs are copied chunk by chunk on copy_in, in the
+ *     query chunks dsa_forward uses;
+ *   - each chunk's kernels run on `stream` once its inputs have arrived;
+ *   - its out / lse rows return on copy_out while later chunks compute.
+ *
+ * The device tensors named in indexer / mla, and out / lse, are caller-owned
+ * device buffers of the full size: they receive the copies and the results.
+ * host_out [total_q, mla n_heads, d_v] and host_lse [total_q, n_heads]
+ * (nullable; needs lse) receive the results.
+ *
+ * Stream order: the call's work starts after the work already enqueued on
+ * `stream`, and work enqueued on `stream` afterwards sees every result,
+ * including the host copies.  copy_in and copy_out may equal `stream` (no
+ * overlap).  Errors as dsa_forward, plus DSA_ERROR_INVALID_VALUE for a
+ * missing host pointer. */
+dsa_status_t dsa_forward_streamed(const dsa_batch_t* batch, const dsa_indexer_t* indexer,
+                                  const dsa_mla_t* mla, int32_t k, const dsa_host_inputs_t* host,
+                                  void* out, float* lse, void* host_out, float* host_lse,
+                                  void* ws, size_t ws_bytes, cudaStream_t stream,
+                                  cudaStream_t copy_in, cudaStream_t copy_out);
+
 /* Synchronises `stream`, then reads and clears the current device's error word
  * (DSA_DEVERR_* bits) into *flags.  Returns DSA_ERROR_TIMEOUT or
  * DSA_ERROR_BAD_INDEX when the corresponding bit was set, else DSA_SUCCESS. */

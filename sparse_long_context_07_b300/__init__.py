@@ -63,6 +63,12 @@ class _Mla(ctypes.Structure):
                 ("kv", ctypes.c_void_p)]
 
 
+class _HostInputs(ctypes.Structure):
+    _fields_ = [("idx_q", ctypes.c_void_p), ("idx_q_scale", ctypes.c_void_p), ("idx_k", ctypes.c_void_p),
+                ("idx_k_scale", ctypes.c_void_p), ("idx_w", ctypes.c_void_p), ("mla_q", ctypes.c_void_p),
+                ("mla_kv", ctypes.c_void_p)]
+
+
 class _Trace(ctypes.Structure):
     _fields_ = [("capacity", ctypes.c_int32), ("count", ctypes.c_int32),
                 ("events", ctypes.POINTER(ctypes.c_void_p)),
@@ -86,6 +92,8 @@ _sig = {
     "dsa_forward": (ctypes.c_int, [_P, _P, _P, ctypes.c_int32, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "dsa_forward_traced": (ctypes.c_int, [_P, _P, _P, ctypes.c_int32, _P, _P, _P, _P, ctypes.c_size_t,
                                           _P, _P]),
+    "dsa_forward_streamed": (ctypes.c_int, [_P, _P, _P, ctypes.c_int32, _P, _P, _P, _P, _P, _P,
+                                            ctypes.c_size_t, _P, _P, _P]),
     "dsa_read_device_errors": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_uint32)]),
     "dsa_debug_inject_fault": (None, [ctypes.c_uint32]),
 }
@@ -297,6 +305,41 @@ def forward(batch: Batch, indexer: Indexer, mla: Mla, k: int, out, lse=None, idx
         st = lib().dsa_forward_traced(_ref(batch), _ref(indexer), _ref(mla), int(k), _ptr(out), _ptr(lse),
                                      _ptr(idx_out), _ptr(ws), nbytes, _stream(stream), ctypes.byref(trace.c))
     _check(st, "dsa_forward")
+
+
+def _host_ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    if t.is_cuda:
+        raise ValueError("host inputs and outputs of forward_streamed must live in host memory")
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to libdsa must be contiguous")
+    return t.data_ptr()
+
+
+class HostInputs:
+    """Host copies (ideally pinned) of an Indexer's and an Mla's tensors, in
+    the same shapes and dtypes, for forward_streamed."""
+
+    def __init__(self, idx_q, idx_k, idx_w, mla_q, mla_kv, idx_q_scale=None, idx_k_scale=None):
+        self.keep = (idx_q, idx_q_scale, idx_k, idx_k_scale, idx_w, mla_q, mla_kv)
+        self.c = _HostInputs(_host_ptr(idx_q), _host_ptr(idx_q_scale), _host_ptr(idx_k), _host_ptr(idx_k_scale),
+                             _host_ptr(idx_w), _host_ptr(mla_q), _host_ptr(mla_kv))
+
+
+def forward_streamed(batch: Batch, indexer: Indexer, mla: Mla, k: int, host: HostInputs, out, lse,
+                     host_out, host_lse=None, ws=None, stream=None, copy_in=None, copy_out=None):
+    """dsa_forward_streamed: inputs copied from host memory chunk by chunk
+    while earlier chunks compute, results copied back to host_out / host_lse.
+    The device tensors of `indexer` / `mla`, `out` and `lse` receive the
+    copies and results; copy_in / copy_out default to `stream`."""
+    nbytes = 0 if ws is None else ws.numel() * ws.element_size()
+    s = _stream(stream)
+    st = lib().dsa_forward_streamed(_ref(batch), _ref(indexer), _ref(mla), int(k), _ref(host), _ptr(out),
+                                    _ptr(lse), _host_ptr(host_out), _host_ptr(host_lse), _ptr(ws), nbytes, s,
+                                    s if copy_in is None else _stream(copy_in),
+                                    s if copy_out is None else _stream(copy_out))
+    _check(st, "dsa_forward_streamed")
 
 
 def read_device_errors(stream=None) -> int:

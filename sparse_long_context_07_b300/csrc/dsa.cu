@@ -704,6 +704,128 @@ dsa_status_t dsa_forward(const dsa_batch_t* batch, const dsa_indexer_t* indexer,
   return dsa_forward_traced(batch, indexer, mla, k, out, lse, idx_out, ws, ws_bytes, stream, nullptr);
 }
 
+dsa_status_t dsa_forward_streamed(const dsa_batch_t* batch, const dsa_indexer_t* indexer, const dsa_mla_t* mla,
+                                  int32_t k, const dsa_host_inputs_t* host, void* out, float* lse, void* host_out,
+                                  float* host_lse, void* ws, size_t ws_bytes, cudaStream_t stream,
+                                  cudaStream_t copy_in, cudaStream_t copy_out) {
+  DSA_TRY(check_batch(batch));
+  DSA_TRY(check_indexer(indexer, batch));
+  DSA_TRY(check_mla(mla, batch));
+  DSA_TRY(check_k(k));
+  if (!host) return fail(DSA_ERROR_INVALID_VALUE, "host inputs are NULL");
+  const bool has_q = batch->total_q > 0, has_kv = batch->total_kv > 0;
+  if ((has_q && (!host->idx_q || !host->idx_w || !host->mla_q || !host_out)) ||
+      (has_kv && (!host->idx_k || !host->mla_kv)) || (!indexer->q_scale != !host->idx_q_scale) ||
+      (!indexer->k_scale != !host->idx_k_scale) || (host_lse && !lse))
+    return fail(DSA_ERROR_INVALID_VALUE,
+                "every device input needs its host copy (scales: both or neither); host_lse needs lse");
+  if ((has_q && !out) || !aligned16(out) || (lse && !aligned16(lse)))
+    return fail(DSA_ERROR_INVALID_VALUE, "out must be non-NULL; out and lse 16-byte aligned");
+  if (ws && !aligned16(ws)) return fail(DSA_ERROR_INVALID_VALUE, "workspace must be 16-byte aligned");
+  DeviceInfo* dev;
+  DSA_TRY(device_info(&dev));
+  if (!has_q) return DSA_SUCCESS;
+  const FwdPlan mn = plan_forward(dev->sms, batch, mla, k, kMinChunk);
+  if (!ws || ws_bytes < mn.total)
+    return fail(DSA_ERROR_INSUFFICIENT_WORKSPACE, "dsa_forward_streamed needs at least %zu bytes of workspace, got %zu",
+                mn.total, ws ? ws_bytes : 0);
+  int64_t lo = mn.chunk, hi = std::min<int64_t>(kPreferredChunk, batch->total_q);
+  if (plan_forward(dev->sms, batch, mla, k, hi).total <= ws_bytes) lo = hi;
+  while (lo < hi) {
+    const int64_t mid = (lo + hi + 1) / 2;
+    if (plan_forward(dev->sms, batch, mla, k, mid).total <= ws_bytes) lo = mid; else hi = mid - 1;
+  }
+  const FwdPlan plan = plan_forward(dev->sms, batch, mla, k, lo);
+  char* wsb = static_cast<char*>(ws);
+  float* scores = reinterpret_cast<float*>(wsb);
+  int32_t* idx_ws = reinterpret_cast<int32_t*>(wsb + plan.scores_bytes);
+  void* mla_ws = plan.mla_bytes ? wsb + plan.scores_bytes + plan.idx_bytes : nullptr;
+
+  // bytes per row of every tensor that moves
+  const size_t ie = indexer->dtype == DSA_DTYPE_E4M3 ? 1 : 4;
+  const size_t me = mla->dtype == DSA_DTYPE_BF16 ? 2 : 4;
+  const size_t row_iq = static_cast<size_t>(indexer->n_heads) * indexer->head_dim * ie;
+  const size_t row_ik = static_cast<size_t>(indexer->head_dim) * ie;
+  const size_t row_w = static_cast<size_t>(indexer->n_heads) * 4;
+  const size_t row_mq = static_cast<size_t>(mla->n_heads) * mla->d_qk * me;
+  const size_t row_kv = static_cast<size_t>(mla->d_qk) * me;
+  const size_t row_out = static_cast<size_t>(mla->n_heads) * mla->d_v * me;
+  const size_t row_lse = static_cast<size_t>(mla->n_heads) * 4;
+
+  // Events order the three streams; each is destroyed once enqueued (its
+  // resources are released when it completes).
+  dsa_status_t st = DSA_SUCCESS;
+  auto event = [&](cudaEvent_t* e) -> bool {
+    if (cudaEventCreateWithFlags(e, cudaEventDisableTiming) != cudaSuccess) {
+      st = fail(DSA_ERROR_LAUNCH, "cudaEventCreate failed: %s", cudaGetErrorString(cudaGetLastError()));
+      return false;
+    }
+    return true;
+  };
+  // one event recorded on `from`, waited for on `to`
+  auto link = [&](cudaStream_t from, cudaStream_t to) -> bool {
+    cudaEvent_t e;
+    if (!event(&e)) return false;
+    const bool ok = cudaEventRecord(e, from) == cudaSuccess && cudaStreamWaitEvent(to, e, 0) == cudaSuccess;
+    cudaEventDestroy(e);
+    if (!ok) st = fail(DSA_ERROR_LAUNCH, "stream ordering failed: %s", cudaGetErrorString(cudaGetLastError()));
+    return ok;
+  };
+  auto h2d = [&](const void* dst, const void* src, size_t bytes, cudaStream_t s) -> bool {
+    if (bytes == 0) return true;
+    if (cudaMemcpyAsync(const_cast<void*>(dst), src, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) {
+      st = fail(DSA_ERROR_LAUNCH, "host-to-device copy failed: %s", cudaGetErrorString(cudaGetLastError()));
+      return false;
+    }
+    return true;
+  };
+  auto d2h = [&](void* dst, const void* src, size_t bytes, cudaStream_t s) -> bool {
+    if (bytes == 0) return true;
+    if (cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess) {
+      st = fail(DSA_ERROR_LAUNCH, "device-to-host copy failed: %s", cudaGetErrorString(cudaGetLastError()));
+      return false;
+    }
+    return true;
+  };
+  auto at = [](const void* base, int64_t row, size_t row_bytes) -> const char* {
+    return static_cast<const char*>(base) + static_cast<size_t>(row) * row_bytes;
+  };
+
+  // start after the work already on `stream`
+  if (!link(stream, copy_in) || !link(stream, copy_out)) return st;
+  // key side in full
+  const int64_t S = batch->total_kv;
+  if (!h2d(indexer->k, host->idx_k, S * row_ik, copy_in) ||
+      (indexer->k_scale && !h2d(indexer->k_scale, host->idx_k_scale, S * 4, copy_in)) ||
+      !h2d(mla->kv, host->mla_kv, S * row_kv, copy_in))
+    return st;
+  Tracer tr{nullptr, stream};
+  for (int64_t r0 = 0; r0 < batch->total_q; r0 += plan.chunk) {
+    const int64_t r1 = std::min<int64_t>(batch->total_q, r0 + plan.chunk);
+    const int64_t nr = r1 - r0;
+    // this chunk's query side
+    if (!h2d(at(indexer->q, r0, row_iq), at(host->idx_q, r0, row_iq), nr * row_iq, copy_in) ||
+        (indexer->q_scale && !h2d(at(indexer->q_scale, r0, 4), at(host->idx_q_scale, r0, 4), nr * 4, copy_in)) ||
+        !h2d(at(indexer->w, r0, row_w), at(host->idx_w, r0, row_w), nr * row_w, copy_in) ||
+        !h2d(at(mla->q, r0, row_mq), at(host->mla_q, r0, row_mq), nr * row_mq, copy_in))
+      return st;
+    if (!link(copy_in, stream)) return st;
+    DSA_TRY(launch_index_scores(*dev, batch, indexer, scores, plan.ld, r0, r1, stream, tr));
+    DSA_TRY(launch_topk(*dev, batch, scores, plan.ld, k, idx_ws, nullptr, r0, r1, stream, tr));
+    char* out_c = static_cast<char*>(out) + static_cast<size_t>(r0) * row_out;
+    float* lse_c = lse ? lse + r0 * mla->n_heads : nullptr;
+    DSA_TRY(launch_sparse_mla(*dev, batch, mla, idx_ws, k, out_c, lse_c, mla_ws, plan.mla_bytes, r0, r1, stream, tr));
+    // this chunk's results back to the host
+    if (!link(stream, copy_out)) return st;
+    if (!d2h(static_cast<char*>(host_out) + static_cast<size_t>(r0) * row_out, out_c, nr * row_out, copy_out) ||
+        (host_lse && !d2h(host_lse + r0 * mla->n_heads, lse_c, nr * row_lse, copy_out)))
+      return st;
+  }
+  // later work on `stream` sees the host copies
+  if (!link(copy_out, stream)) return st;
+  return DSA_SUCCESS;
+}
+
 dsa_status_t dsa_read_device_errors(cudaStream_t stream, uint32_t* flags) {
   DeviceInfo* dev;
   DSA_TRY(device_info(&dev));
