@@ -302,14 +302,10 @@ def main():
     clk = clocks.stop()
     if world > 1:
         dist.barrier()
-    ms = ev0.elapsed_time(ev1)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ev0.elapsed_time(ev1), world, dev)
     ms_per_step = ms / a.steps
     tokens_per_step = T * world
-    value = tokens_per_step / (ms_per_step / 1e3)
+    value = job_rate(tokens_per_step, ms_per_step)
 
     # per-kernel durations from the launch trace
     per_kernel = {}
@@ -378,6 +374,24 @@ def summarize(lens):
     if len(set(lens)) == 1:
         return f"{len(lens)}x{lens[0]}"
     return f"{len(lens)} seqs, {min(lens)}..{max(lens)}, total {sum(lens)}"
+
+
+def max_over_ranks(value, world, device):
+    """The largest of every rank's value: the job's step time is that of its
+    slowest rank.  `device` holds the reduction tensor (the GPU under NCCL,
+    the CPU under gloo)."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(tokens_all_ranks, ms_per_step):
+    """Whole-job throughput: every rank's tokens over the slowest rank's time."""
+    return tokens_all_ranks / (ms_per_step / 1e3)
 
 
 def reseed(wl, rank, dev):
@@ -573,13 +587,8 @@ def measure_e2e(a, wl, dsa, b, ix, m, out, lse, ws, stream, world, dev):
         step()
     ev1.record(stream)
     torch.cuda.synchronize()
-    ms = ev0.elapsed_time(ev1) / n
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    return {"value": wl.total_q * world / (ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+    ms = max_over_ranks(ev0.elapsed_time(ev1) / n, world, dev)
+    return {"value": job_rate(wl.total_q * world, ms), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": n,
             "api": "dsa_forward_streamed (copies overlap the kernels, query chunk by chunk)"}
 
