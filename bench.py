@@ -41,14 +41,15 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--workload", default="prefill128k")
-    ap.add_argument("--e2e-steps", type=int, default=2)
+    ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle cpu_baseline leg")
-    ap.add_argument("--cpu-seconds", type=float, default=25.0, help="target oracle time per sample")
+    ap.add_argument("--cpu-seconds", type=float, default=24.0,
+                    help="oracle time of the cpu_baseline leg (split between all cores and one thread)")
     ap.add_argument("--decode-steps", type=int, default=10,
                     help="timed steps of the ragged 128K decode measurement (0 = skip)")
     ap.add_argument("--dense-steps", type=int, default=1,
@@ -183,49 +184,64 @@ class ClockSampler:
 # ----------------------------------------------------------------------------
 # oracle timing (cpu_baseline and the reference arm)
 # ----------------------------------------------------------------------------
-def oracle_sample(wl, target_s, seed=0):
-    """Time the fp64 oracle on evenly spaced query rows of the workload.
-    Returns (tokens/s extrapolated to the whole workload, description, threads)."""
+def oracle_sample(wl, target_s, seed=0, threads=None):
+    """Time the fp64 oracle on evenly spaced query rows of the workload (the
+    grid of rows is shifted by a seeded offset, so different seeds time
+    different rows).  `threads` limits the BLAS threads (None: all).
+    Returns (tokens/s extrapolated to the whole workload, description, seconds
+    measured, threads used)."""
     import oracle
+    from threadpoolctl import threadpool_limits
     from tests.helpers import cu_np, idx_real, mla_real
 
     cu_q, cu_kv = cu_np(wl)
     _, pos, kv0, n = oracle.query_positions(cu_q, cu_kv)
     T = len(n)
     w_all = wl.w.float().cpu().numpy().astype(np.float64)
-    # decode of the key rows is per sequence, timed once and charged in full
-    t0 = time.perf_counter()
-    k_all = idx_real(wl, "k")
-    kv_dec = None
-    t_decode = time.perf_counter() - t0
+    with threadpool_limits(limits=threads, user_api="blas"):
+        used = blas_threads()
+        # decode of the key rows is per sequence, timed once and charged in full
+        t0 = time.perf_counter()
+        k_all = idx_real(wl, "k")
+        t_decode = time.perf_counter() - t0
 
-    def one(r):
-        q = idx_real(wl, "q", [r])[0]
-        I = oracle.index_scores_row(q, k_all[kv0[r]:kv0[r] + n[r]], w_all[r])
-        sel = oracle.topk_indices(I, wl.topk)
-        valid = sel[sel >= 0]
-        Q = mla_real(wl.Q, [r])[0]
-        kv = mla_real(wl.KV, kv0[r] + valid)
-        oracle.sparse_mla_row(Q, kv, np.arange(len(valid)), wl.scale, wl.d_v)
+        def one(r):
+            q = idx_real(wl, "q", [r])[0]
+            I = oracle.index_scores_row(q, k_all[kv0[r]:kv0[r] + n[r]], w_all[r])
+            sel = oracle.topk_indices(I, wl.topk)
+            valid = sel[sel >= 0]
+            Q = mla_real(wl.Q, [r])[0]
+            kv = mla_real(wl.KV, kv0[r] + valid)
+            oracle.sparse_mla_row(Q, kv, np.arange(len(valid)), wl.scale, wl.d_v)
 
-    # probe the per-row cost on the middle row (second, warm call), then size
-    # the sample
-    one(T // 2)
-    t0 = time.perf_counter()
-    one(T // 2)
-    probe = time.perf_counter() - t0
-    R = int(max(4, min(T, target_s / max(probe, 1e-4))))
-    rows = np.unique(((np.arange(R) + 0.5) * T / R).astype(np.int64))
-    t0 = time.perf_counter()
-    for r in rows:
-        one(int(r))
-    el = time.perf_counter() - t0
+        # probe the per-row cost on the middle row (second, warm call), then
+        # size the sample
+        one(T // 2)
+        t0 = time.perf_counter()
+        one(T // 2)
+        probe = time.perf_counter() - t0
+        R = int(max(4, min(T, target_s / max(probe, 1e-4))))
+        off = np.random.default_rng(seed).random() if seed else 0.5
+        rows = np.unique(np.minimum(T - 1, ((np.arange(R) + off) * T / R).astype(np.int64)))
+        t0 = time.perf_counter()
+        for r in rows:
+            one(int(r))
+        el = time.perf_counter() - t0
     per_row = el / len(rows)
     total_s = t_decode + per_row * T
-    desc = (f"{len(rows)} evenly spaced query rows of {wl.name} (T={T}); per-row oracle time "
-            f"x T + one decode of the key cache, {el + t_decode:.1f} s measured")
-    del kv_dec
-    return T / total_s, desc, el + t_decode
+    desc = (f"{len(rows)} evenly spaced query rows of {wl.name} (T={T}, offset {off:.3f}); per-row oracle "
+            f"time x T + one decode of the key cache, {el + t_decode:.1f} s measured, {used} BLAS thread(s)")
+    return T / total_s, desc, el + t_decode, used
+
+
+def cpu_baseline(wl, seconds):
+    """The oracle on all host cores and on one thread (each about half of
+    `seconds`); `value` is the all-core figure."""
+    tps, desc, _, used = oracle_sample(wl, seconds / 2)
+    tps1, desc1, _, _ = oracle_sample(wl, seconds / 2, seed=1, threads=1)
+    return {"value": tps, "unit": "tokens/s", "cores": used, "kind": "oracle", "sample": desc,
+            "single_thread": {"value": tps1, "unit": "tokens/s", "cores": 1, "sample": desc1},
+            "host_cpus": os.cpu_count()}
 
 
 def blas_threads():
@@ -293,17 +309,19 @@ def main():
         dist.barrier()
     torch.cuda.synchronize()
     clocks.start()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ev0.record(stream)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(a.steps + 1)]
+    evs[0].record(stream)
     for i in range(a.steps):
         step(traces[i])
-    ev1.record(stream)
+        evs[i + 1].record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
     if world > 1:
         dist.barrier()
-    ms = max_over_ranks(ev0.elapsed_time(ev1), world, dev)
-    ms_per_step = ms / a.steps
+    per_step = [evs[i].elapsed_time(evs[i + 1]) for i in range(a.steps)]
+    # the median step of the slowest rank; the mean of all K steps beside it
+    ms_per_step = max_over_ranks(statistics.median(per_step), world, dev)
+    ms_mean = max_over_ranks(evs[0].elapsed_time(evs[-1]) / a.steps, world, dev)
     tokens_per_step = T * world
     value = job_rate(tokens_per_step, ms_per_step)
 
@@ -317,6 +335,8 @@ def main():
             d[1] += 1
             launches += 1
     roof = roofline(wl, per_kernel, a.steps)
+    if roof is not None:
+        roof["launch_ms_note"] = "per-kernel CUDA-event times summed over the K timed steps"
 
     e2e = None
     if not a.no_e2e:
@@ -332,13 +352,14 @@ def main():
         torch.cuda.empty_cache()
         decode = measure_decode(a, dsa, dev, stream)
         decode["quantize"] = measure_quant(a, dsa, dev, stream)
+        if roof is not None:
+            roof["kernels"] += decode_rooflines(decode)
 
     if rank != 0:
         return
     cpu = None
     if world == 1 and not a.no_cpu:
-        tps, desc, secs = oracle_sample(wl, a.cpu_seconds)
-        cpu = {"value": tps, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle", "sample": desc}
+        cpu = cpu_baseline(wl, a.cpu_seconds)
     line = {
         "metric": METRIC,
         "value": value,
@@ -347,6 +368,8 @@ def main():
         "steps": a.steps,
         "warmup": max(3, a.warmup),
         "ms_per_step": ms_per_step,
+        "ms_per_step_mean": ms_mean,
+        "timing": "median of K per-step CUDA-event times (max over ranks); mean beside it",
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -395,42 +418,90 @@ def job_rate(tokens_all_ranks, ms_per_step):
 
 
 def reseed(wl, rank, dev):
+    """Rank `rank`'s replica: the workload's own recipe with another seed."""
     import dsa_synth
-    return dsa_synth.make_workload(wl.name, wl.seqlens_q, wl.seqlens_kv, seed=1000 + rank, device=dev)
+    return dsa_synth.reseeded(wl, 1000 + rank, dev)
+
+
+def _peaks():
+    """(peaks dict with the e4m3 figures derived, source label).  e4m3 dense
+    = 2 x the measured bf16 cuBLAS rate (the nominal fp8:bf16 ratio)."""
+    peaks, src = load_peaks()
+    burst = peaks.get("bf16_tflops")
+    sus = peaks.get("bf16_tflops_sustained", burst)
+    return {"bf16_burst": burst, "bf16_sustained": sus, "e4m3_burst": 2.0 * burst,
+            "e4m3_sustained": 2.0 * sus, "hbm": peaks.get("hbm_gbs")}, src
+
+
+def _entry(kernel, bound, unit, work, seconds, pk, peak_key, src, extra=None):
+    """One roofline entry: algorithmic work over measured time against the
+    sustained (timed inside a long step) and the burst peak."""
+    achieved = work / seconds / (1e12 if unit == "TFLOP/s" else 1e9)
+    if peak_key == "hbm":
+        sus = burst = pk["hbm"]
+        note = f"{src} copy bandwidth"
+    else:
+        sus, burst = pk[peak_key + "_sustained"], pk[peak_key + "_burst"]
+        note = (f"{src} cuBLAS bf16" if peak_key == "bf16" else f"2 x {src} cuBLAS bf16 (e4m3 dense)") + \
+            " rate; frac against the sustained figure, frac_burst against the burst one"
+    e = {"kernel": kernel, "bound": bound, "unit": unit, "achieved": achieved, "peak": sus,
+         "frac": achieved / sus, "peak_burst": burst, "frac_burst": achieved / burst, "peak_note": note}
+    if extra:
+        e.update(extra)
+    return e
 
 
 def roofline(wl, per_kernel, steps):
-    """Roofline of the dominant kernel: algorithmic work of all its launches
-    over their total CUDA-event time, against the measured peak."""
+    """Roofline of every kernel of the step: algorithmic work of all its
+    launches over their total CUDA-event time, against the measured peaks.
+    The top-level fields are those of the dominant kernel (largest total
+    time); `kernels` lists all of them."""
     if not per_kernel:
         return None
-    peaks, src = load_peaks()
+    pk, src = _peaks()
     wm = work_model(wl)
     allrows = np.arange(len(wm["n"]))
-    name = max(per_kernel, key=lambda kk: per_kernel[kk][0])
-    tot_ms, nl = per_kernel[name]
     traffic_tab = load_traffic()
-    if name.startswith("indexer"):
-        work = wm["indexer_flops"](allrows) * steps
-        achieved = work / (tot_ms / 1e3) / 1e12
-        peak = 2.0 * peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
-        res = {"bound": "tensor", "unit": "TFLOP/s", "kernel": name,
-               "peak_note": f"e4m3 dense = 2 x {src} sustained bf16 cuBLAS"}
-    elif name.startswith("mla"):
-        work = wm["mla_flops"](allrows) * steps
-        achieved = work / (tot_ms / 1e3) / 1e12
-        peak = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
-        res = {"bound": "tensor", "unit": "TFLOP/s", "kernel": name, "peak_note": f"{src} sustained bf16 cuBLAS"}
-    else:
-        work = wm["topk_bytes"](allrows) * steps
-        achieved = work / (tot_ms / 1e3) / 1e9
-        peak = peaks.get("hbm_gbs")
-        res = {"bound": "hbm", "unit": "GB/s", "kernel": name, "peak_note": f"{src} copy bandwidth"}
-    tr = traffic_tab.get(name, {}).get(wl.name)
-    res.update({"achieved": achieved, "peak": peak, "frac": achieved / peak,
-                "traffic": (tr * nl / steps / max(1, nl / steps)) if tr else None,
-                "launches_per_step": nl / steps, "ms_per_step": tot_ms / steps})
+    entries = []
+    for name, (tot_ms, nl) in per_kernel.items():
+        extra = {"ms_per_step": tot_ms / steps, "launches_per_step": nl / steps, "workload": wl.name}
+        secs = tot_ms / 1e3
+        if name.startswith("indexer"):
+            e = _entry(name, "tensor", "TFLOP/s", wm["indexer_flops"](allrows) * steps, secs, pk, "e4m3", src, extra)
+        elif name == "mla_tc" or name == "mla_simt":
+            e = _entry(name, "tensor", "TFLOP/s", wm["mla_flops"](allrows) * steps, secs, pk, "bf16", src, extra)
+        elif name == "topk":
+            e = _entry(name, "hbm", "GB/s", wm["topk_bytes"](allrows) * steps, secs, pk, "hbm", src, extra)
+        else:
+            continue
+        tr = traffic_tab.get(name, {}).get(wl.name)
+        e["traffic"] = tr if tr else None
+        entries.append(e)
+    if not entries:
+        return None
+    dom = max(entries, key=lambda e: e["ms_per_step"])
+    res = {k: dom[k] for k in ("bound", "achieved", "peak", "unit", "frac", "traffic", "kernel", "peak_burst",
+                               "frac_burst", "peak_note", "ms_per_step", "launches_per_step")}
+    res["kernels"] = entries
     return res
+
+
+def decode_rooflines(decode):
+    """The ragged 128K decode's HBM-bound kernels as roofline entries."""
+    out = []
+    pk, src = _peaks()
+    for key, kernel in (("mla_hbm", "mla_tc+combine (decode)"), ("indexer_hbm", "indexer_tc (decode)")):
+        d = decode.get(key)
+        if not d:
+            continue
+        ms = d["ms"]
+        out.append(_entry(kernel, "hbm", "GB/s", d["bytes"], ms / 1e3, pk, "hbm", src,
+                          {"ms_per_step": ms, "workload": decode["workload"], "l2": "flushed before every step"}))
+    q = decode.get("quantize")
+    if q:
+        out.append(_entry("quantize_e4m3", "hbm", "GB/s", q["bytes"], q["ms"] / 1e3, pk, "hbm", src,
+                          {"ms_per_step": q["ms"], "workload": q["workload"]}))
+    return out
 
 
 def measure_decode(a, dsa, dev, stream):
@@ -498,11 +569,12 @@ def measure_decode(a, dsa, dev, stream):
     if mla_ms > 0:
         gbs = mla_bytes / (mla_ms / 1e3) / 1e9
         res["mla_hbm"] = {"achieved": gbs, "peak": peaks.get("hbm_gbs"), "unit": "GB/s",
-                          "frac": gbs / peaks.get("hbm_gbs"), "bytes": mla_bytes, "note": f"{src} copy bandwidth"}
+                          "frac": gbs / peaks.get("hbm_gbs"), "bytes": mla_bytes, "ms": mla_ms,
+                          "note": f"{src} copy bandwidth"}
     if kms.get("indexer_tc"):
         gbs = idx_bytes / (kms["indexer_tc"] / 1e3) / 1e9
         res["indexer_hbm"] = {"achieved": gbs, "peak": peaks.get("hbm_gbs"), "unit": "GB/s",
-                              "frac": gbs / peaks.get("hbm_gbs"), "bytes": idx_bytes}
+                              "frac": gbs / peaks.get("hbm_gbs"), "bytes": idx_bytes, "ms": kms["indexer_tc"]}
     return res
 
 
@@ -581,15 +653,17 @@ def measure_e2e(a, wl, dsa, b, ix, m, out, lse, ws, stream, world, dev):
     step()
     torch.cuda.synchronize()
     n = max(1, a.e2e_steps)
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ev0.record(stream)
-    for _ in range(n):
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+    evs[0].record(stream)
+    for i in range(n):
         step()
-    ev1.record(stream)
+        evs[i + 1].record(stream)
     torch.cuda.synchronize()
-    ms = max_over_ranks(ev0.elapsed_time(ev1) / n, world, dev)
+    per_step = [evs[i].elapsed_time(evs[i + 1]) for i in range(n)]
+    ms = max_over_ranks(statistics.median(per_step), world, dev)
+    ms_mean = max_over_ranks(evs[0].elapsed_time(evs[-1]) / n, world, dev)
     return {"value": job_rate(wl.total_q * world, ms), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": n,
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms, "ms_per_step_mean": ms_mean, "steps": n,
             "api": "dsa_forward_streamed (copies overlap the kernels, query chunk by chunk)"}
 
 
@@ -604,13 +678,14 @@ def run_reference(a, world):
     for _ in range(max(0, a.warmup)):
         pass  # the oracle has no state to warm up
     vals, descs, secs = [], [], []
+    cores = blas_threads()
     for i in range(a.steps):
-        tps, desc, s = oracle_sample(wl, max(1.0, a.cpu_seconds / max(1, a.steps)), seed=i)
+        # each step times a different seeded grid of rows
+        tps, desc, s, cores = oracle_sample(wl, max(1.0, a.cpu_seconds / max(1, a.steps)), seed=i + 1)
         vals.append(tps)
         descs.append(desc)
         secs.append(s)
     value = statistics.median(vals)
-    cores = blas_threads()
     line = {
         "impl": "reference",
         "metric": METRIC,

@@ -53,6 +53,9 @@ class Workload:
     scale: float
     d_v: int
     topk: int
+    # every keyword argument of make_workload that drew this workload, so
+    # that a replica with another seed (reseeded) has the same recipe
+    gen_kwargs: dict = dataclasses.field(default_factory=dict)
 
     @property
     def total_q(self) -> int:
@@ -135,6 +138,9 @@ def make_workload(name, seqlens_q, seqlens_kv, *, n_idx_heads=64, idx_dim=128,
     fraction of each sequence's keys toward the sequence's last query (the
     direction sum_j w_j q_j, normalised to norm sqrt(d_I)) before quantisation.
     Large tensors are drawn in row chunks to bound temporary memory."""
+    gen_kwargs = dict(n_idx_heads=n_idx_heads, idx_dim=idx_dim, idx_dtype=idx_dtype, n_heads=n_heads,
+                      d_qk=d_qk, d_v=d_v, mla_dtype=mla_dtype, topk=topk, scale=scale, seed=seed,
+                      grid=grid, planted=planted, w_std=w_std, chunk_rows=chunk_rows)
     device = torch.device(device)
     gen = torch.Generator(device=device)
     gen.manual_seed(int(seed))
@@ -208,7 +214,15 @@ def make_workload(name, seqlens_q, seqlens_kv, *, n_idx_heads=64, idx_dim=128,
                     cu_q=_cu(seqlens_q, device), cu_kv=_cu(seqlens_kv, device),
                     idx_dtype=idx_dtype, q_idx=q_idx, q_scale=q_scale, k_idx=k_idx,
                     k_scale=k_scale, w=w, mla_dtype=mla_dtype, Q=Q, KV=KV,
-                    scale=float(scale), d_v=int(d_v), topk=int(topk))
+                    scale=float(scale), d_v=int(d_v), topk=int(topk), gen_kwargs=gen_kwargs)
+
+
+def reseeded(wl: Workload, seed: int, device) -> Workload:
+    """The same recipe as `wl` (lengths, dimensions, dtypes, grid, planted
+    fraction, ...) drawn with another seed: an independent replica."""
+    kw = dict(wl.gen_kwargs)
+    kw["seed"] = int(seed)
+    return make_workload(wl.name, wl.seqlens_q, wl.seqlens_kv, device=device, **kw)
 
 
 def ragged_lengths(batch, lo, hi, seed):

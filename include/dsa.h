@@ -192,10 +192,14 @@ dsa_status_t dsa_sparse_mla(const dsa_batch_t* batch, const dsa_mla_t* mla, cons
  * results and errors as dsa_sparse_mla, minus ws/ws_bytes: the split-KV
  * partials of small decode batches live in a 24 MiB array compiled into the
  * library, which every GPU that loads the library holds until the process
- * exits.  A batch whose split plan needs more than 24 MiB (on a 148-SM B300
- * with k = 2048: decode batches of 24 or of 32 to 36 query rows) is rejected
- * with DSA_ERROR_NOT_SUPPORTED;
- * call dsa_sparse_mla with a workspace for those.  The first call on each
+ * exits.  A batch whose preferred split needs more than 24 MiB (on a 148-SM
+ * B300 with k = 2048: decode batches of 24 or of 32 to 36 query rows) splits
+ * each row over fewer CTA pairs so that its partials fit, down to no split at
+ * all; its results then agree with dsa_sparse_mla's to float rounding, not
+ * bit for bit.  A plan that still did not fit would be refused with
+ * DSA_ERROR_NOT_SUPPORTED (call dsa_sparse_mla with a workspace then); with
+ * the split count able to fall to one, no batch of the tensor-core instance
+ * is refused for its size.  The first call on each
  * device looks up the array's device address (cudaGetSymbolAddress), so make
  * that first call before any stream capture.  Every call shares the one
  * array and it keeps the last call's contents; the kernels overwrite

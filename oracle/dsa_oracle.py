@@ -18,7 +18,7 @@ Sources ("the pages"):
        pages only say "FP8"; the e4m3 variant and the per-token fp32 scales are
        the workload's stated input format.
 
-Readings taken where the pages are silent (each is listed in the design doc):
+Readings taken where the pages are silent (each also listed in the design notes):
   * Causal domain: query at position p sees keys s in [0, p] (self included).
   * Ragged batches are bottom-right aligned: query i of a sequence with nq
     queries and nkv keys sits at p = nkv - nq + i.

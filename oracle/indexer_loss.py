@@ -13,7 +13,7 @@ Sources:
        KL divergence between the aggregated dense attention scores,
        L1-normalised, and the indexer outputs.
 
-Readings taken where the pages are silent (each is listed in the design doc):
+Readings taken where the pages are silent (each also listed in the design notes):
   * "Aggregated dense attention scores": the per-head softmax distributions
     of the main (MLA-MQA) attention over the causal candidates s = 0..p,
     summed over the heads; L1 normalisation then divides by their sum, H.

@@ -234,7 +234,7 @@ def sparse_mla_noalloc(batch: Batch, mla: Mla, idx, k: int, out, lse=None, strea
     """dsa_sparse_mla without a workspace argument, for callers that cannot
     allocate device scratch: its split-KV partials live in a fixed 24 MiB array
     inside the library (shared by all calls; overlapping calls race).  Batches
-    needing more than that raise DSAError (ERROR_NOT_SUPPORTED)."""
+    whose preferred split would need more take fewer splits."""
     _check(lib().dsa_sparse_mla_noalloc(_ref(batch), _ref(mla), _ptr(idx), int(k), _ptr(out), _ptr(lse),
                                         _stream(stream)), "dsa_sparse_mla_noalloc")
 

@@ -612,8 +612,10 @@ dsa_status_t dsa_sparse_mla_noalloc(const dsa_batch_t* batch, const dsa_mla_t* m
     return fail(DSA_ERROR_INVALID_VALUE, "idx and out must be non-NULL and 16-byte aligned");
   DeviceInfo* dev;
   DSA_TRY(device_info(&dev));
-  // the same split plan dsa_sparse_mla would use with an unlimited workspace
-  const size_t need = mla_is_tc(mla) ? plan_mla(dev->sms, batch->total_q, k).ws_bytes : 0;
+  // the split plan dsa_sparse_mla uses with a workspace of the built-in
+  // scratch's size: a batch whose preferred split would not fit takes fewer
+  // splits, so only a plan that cannot shrink below the array is refused
+  const size_t need = mla_is_tc(mla) ? plan_mla(dev->sms, batch->total_q, k, kStaticScratchBytes).ws_bytes : 0;
   if (need > kStaticScratchBytes)
     return fail(DSA_ERROR_NOT_SUPPORTED,
                 "dsa_sparse_mla_noalloc: this batch needs %zu bytes of split-KV scratch but the built-in "
@@ -641,15 +643,20 @@ dsa_status_t dsa_quantize_e4m3(const void* x, dsa_dtype_t x_dtype, int64_t group
   DeviceInfo* dev;
   DSA_TRY(device_info(&dev));
   const bool bf16 = x_dtype == DSA_DTYPE_BF16;
-  const int64_t per_cta = dsa::quant::kThreads / 32;   // one warp per group
-  const int64_t ctas = (groups + per_cta - 1) / per_cta;
-  if (ctas > 2147483647ll) return fail(DSA_ERROR_NOT_SUPPORTED, "quantize: too many groups");
-  if (group_elems <= dsa::quant::kWarpGroupMax)
+  if (group_elems <= dsa::quant::kWarpGroupMax) {
+    const int64_t per_cta = dsa::quant::kThreads / 32;   // one warp per group
+    const int64_t ctas = (groups + per_cta - 1) / per_cta;
     dsa::quant::quantize_warp_kernel<<<static_cast<unsigned>(ctas), dsa::quant::kThreads, 0, stream>>>(
         x, bf16, groups, group_elems, codes, scales);
-  else
-    dsa::quant::quantize_stream_kernel<<<static_cast<unsigned>(ctas), dsa::quant::kThreads, 0, stream>>>(
-        x, bf16, groups, group_elems, codes, scales);
+  } else {
+    // one CTA per group (groups < 2^31 was checked above)
+    if (bf16)
+      dsa::quant::quantize_cta_kernel<true><<<static_cast<unsigned>(groups), dsa::quant::CtaShape<true>::kThreads,
+                                              0, stream>>>(x, group_elems, codes, scales);
+    else
+      dsa::quant::quantize_cta_kernel<false><<<static_cast<unsigned>(groups), dsa::quant::CtaShape<false>::kThreads,
+                                               0, stream>>>(x, group_elems, codes, scales);
+  }
   return check_launch("quantize_e4m3");
 }
 

@@ -33,11 +33,14 @@ def run_forward(wl, k, ws_bytes=None):
     return out, lse, idx
 
 
-def check_rows(wl, k, out, lse, idx, rows, exact_sets, what):
-    cache = {}
+def check_rows(wl, k, out, lse, idx, rows, exact_sets, what, cache=None):
+    """Selection of each row against the oracle's top-k (bit-exact, or the
+    near-tie set rule), then the oracle's attention over the set the GPU
+    returned (once that set has passed) against the GPU's output."""
+    cache = {} if cache is None else cache
     scores = oracle_scores_cached(wl, rows, cache)
     gi = idx.cpu().numpy()
-    same_set_rows = []
+    gpu_sets = []
     for i, r in enumerate(rows):
         ref = oracle.topk_indices(scores[i], k)
         if exact_sets:
@@ -45,10 +48,12 @@ def check_rows(wl, k, out, lse, idx, rows, exact_sets, what):
         else:
             ok, nd = set_rule_ok(gi[r], ref, scores[i], k)
             assert ok, f"{what}: row {r} selection differs beyond near-ties ({nd})"
-            assert np.all(np.diff(gi[r][gi[r] >= 0]) > 0)
-        same_set_rows.append(ref)
-    # attention of the oracle on its own selection
-    ref_o, ref_l = oracle_attention(wl, rows, same_set_rows)
+            valid = gi[r][gi[r] >= 0]
+            assert np.all(np.diff(valid) > 0), f"{what}: row {r} not ascending"
+            assert np.all(gi[r][len(valid):] == -1), f"{what}: row {r} padding"
+        gpu_sets.append(gi[r])
+    # attention of the oracle over the GPU's selection
+    ref_o, ref_l = oracle_attention(wl, rows, gpu_sets)
     assert_attention_close(to_f64(out[rows]), ref_o, what)
     assert_lse_close(to_f64(lse[rows]), ref_l, what)
 
@@ -127,12 +132,67 @@ def test_forward_misaligned_pointer_rejected():
     assert e.value.status == dsa.ERROR_INVALID_VALUE
 
 
-@pytest.mark.parametrize("name,nrows", [("prefill32k", 10), ("ragged128k", 8), ("prefill128k", 6)])
-def test_forward_full_size_sampled(name, nrows):
-    wl = dsa_synth.WORKLOADS[name](device="cuda")
+def test_forward_decode8k_integer_grid_exact_sets():
+    # production dims, k = 2048 over 8192 candidates: the cluster top-k path
+    wl = dsa_synth.decode8k(device="cuda", grid=True)
+    out, lse, idx = run_forward(wl, wl.topk)
+    check_rows(wl, wl.topk, out, lse, idx, list(range(wl.total_q)), True, "decode8k grid")
+
+
+def test_forward_prefill32k_integer_grid_exact_sets():
+    # k = 2048 over up to 32768 candidates, two 16384-row chunks of the
+    # forward's workspace: selections bit-exact on both sides of every boundary
+    wl = dsa_synth.prefill32k(device="cuda", grid=True)
     out, lse, idx = run_forward(wl, wl.topk)
     T = wl.total_q
-    rows = sample_rows(T, nrows, seed=7, must=[0, T - 1] + ([2047, 2048] if T > 2048 else []))
-    check_rows(wl, wl.topk, out, lse, idx, rows, False, name)
+    must = [0, 1, 2046, 2047, 2048, 2049, 4095, 4096, 16383, 16384, 16385, 24576, T - 2, T - 1]
+    rows = sample_rows(T, 56, seed=3, must=must)
+    assert len(rows) >= 64
+    check_rows(wl, wl.topk, out, lse, idx, rows, True, "prefill32k grid")
+    del wl, out, lse, idx
+    torch.cuda.empty_cache()
+
+
+def test_forward_ragged128k_every_row():
+    # all 64 decode rows (contexts of 16K to 128K, planted keys)
+    wl = dsa_synth.WORKLOADS["ragged128k"](device="cuda")
+    out, lse, idx = run_forward(wl, wl.topk)
+    check_rows(wl, wl.topk, out, lse, idx, list(range(wl.total_q)), False, "ragged128k")
+    del wl, out, lse, idx
+    torch.cuda.empty_cache()
+
+
+def stratified_rows(T, count, seed, must):
+    """`must` plus one seeded row from each of `count` equal strata of [0, T)."""
+    g = np.random.default_rng(seed)
+    edges = np.linspace(0, T, count + 1).astype(np.int64)
+    rows = {int(g.integers(edges[i], max(edges[i] + 1, edges[i + 1]))) for i in range(count)}
+    rows |= {int(r) for r in must if 0 <= r < T}
+    return sorted(rows)
+
+
+def test_forward_prefill32k_sampled():
+    wl = dsa_synth.prefill32k(device="cuda")
+    out, lse, idx = run_forward(wl, wl.topk)
+    T = wl.total_q
+    rows = stratified_rows(T, 64, seed=7, must=[0, 1, 2047, 2048, 2049, 16383, 16384, T - 1])
+    check_rows(wl, wl.topk, out, lse, idx, rows, False, "prefill32k")
+    del wl, out, lse, idx
+    torch.cuda.empty_cache()
+
+
+def test_forward_prefill128k_sampled():
+    # the bench workload in the bench's launch configuration (preferred
+    # workspace: 16384-row chunks); >= 256 rows including both sides of every
+    # chunk boundary
+    wl = dsa_synth.WORKLOADS["prefill128k"](device="cuda")
+    out, lse, idx = run_forward(wl, wl.topk)
+    T = wl.total_q
+    must = [0, 1, 2047, 2048, 2049, T - 1]
+    for c in range(16384, T, 16384):
+        must += [c - 1, c]
+    rows = stratified_rows(T, 240, seed=5, must=must)
+    assert len(rows) >= 256
+    check_rows(wl, wl.topk, out, lse, idx, rows, False, "prefill128k")
     del wl, out, lse, idx
     torch.cuda.empty_cache()

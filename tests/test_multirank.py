@@ -66,3 +66,27 @@ def test_replicas_draw_independent_inputs():
     assert torch.equal(a1.Q, b1.Q) and torch.equal(a1.k_idx, b1.k_idx)
     assert not torch.equal(a1.Q, a2.Q)
     assert a1.Q.shape == wl.Q.shape and a1.total_q == wl.total_q
+
+
+def test_replicas_keep_the_workload_recipe():
+    # planted keys, non-default dimensions and dtypes survive the reseed
+    sys.path.insert(0, ROOT)
+    import bench
+    import dsa_synth
+    wl = dsa_synth.make_workload("replica-planted", [1, 1], [300, 200], device="cpu", seed=8, planted=0.10,
+                                 n_idx_heads=4, idx_dim=32, idx_dtype="f32", n_heads=8, d_qk=64, d_v=64,
+                                 mla_dtype="f32", topk=32, scale=0.125)
+    r = bench.reseed(wl, 1, "cpu")
+    assert r.gen_kwargs == {**wl.gen_kwargs, "seed": 1001}
+    assert r.gen_kwargs["planted"] == 0.10
+    for name in ("q_idx", "k_idx", "w", "Q", "KV"):
+        a, b = getattr(wl, name), getattr(r, name)
+        assert a.shape == b.shape and a.dtype == b.dtype, name
+        assert not torch.equal(a, b), name
+    assert (r.topk, r.scale, r.d_v, r.idx_dtype, r.mla_dtype) == (wl.topk, wl.scale, wl.d_v, wl.idx_dtype, wl.mla_dtype)
+    tiny = dsa_synth.tiny(device="cpu", grid=True)
+    rt = bench.reseed(tiny, 1, "cpu")
+    assert rt.n_idx_heads == 4 and rt.idx_dim == 32 and rt.n_heads == 8 and rt.topk == 32
+    assert rt.gen_kwargs["grid"] is True
+    # grid values stay on the integer grid
+    assert torch.equal(rt.q_idx, rt.q_idx.round()) and rt.q_idx.abs().max() <= 2

@@ -327,6 +327,54 @@ def test_dense_equivalence_when_k_covers_context():
     assert np.allclose(out_s[:4], ref[:4]) and not np.allclose(out_s[-1], ref[-1])
 
 
+def _sdpa_bottom_right(Q, KV, scale, d_v):
+    """Dense MQA attention of one sequence with torch's library SDPA in fp64:
+    nq queries over nkv keys, query i seeing keys 0 .. nkv - nq + i (an
+    explicit boolean mask, so no causal convention of the library is used)."""
+    nq, H, d = Q.shape
+    nkv = KV.shape[0]
+    allowed = np.arange(nkv)[None, :] <= (nkv - nq + np.arange(nq))[:, None]
+    q = torch.from_numpy(Q).permute(1, 0, 2)[None]
+    kk = torch.from_numpy(KV)[None, None].expand(1, H, nkv, d)
+    vv = torch.from_numpy(KV[:, :d_v])[None, None].expand(1, H, nkv, d_v)
+    o = torch.nn.functional.scaled_dot_product_attention(q, kk, vv, attn_mask=torch.from_numpy(allowed),
+                                                         scale=scale)
+    return o[0].permute(1, 0, 2).numpy()
+
+
+def test_two_sequence_batch_against_per_sequence_dense_attention():
+    # a 10-token prefill and a 6-token chunk appended to 9 cached tokens: with
+    # k covering every candidate, forward_rows and sparse_mla over the whole
+    # ragged batch must equal dense attention computed on each sequence's own
+    # slice, so a wrong key offset of the second sequence fails here
+    rng = np.random.default_rng(12)
+    nq, nkv = [10, 6], [10, 15]
+    cu_q, cu_kv = np.array([0, 10, 16]), np.array([0, 10, 25])
+    T, S, HI, dI, H, d, dv = 16, 25, 3, 8, 4, 16, 12
+    q = rng.standard_normal((T, HI, dI))
+    k = rng.standard_normal((S, dI))
+    w = rng.standard_normal((T, HI))
+    Q = rng.standard_normal((T, H, d))
+    KV = rng.standard_normal((S, d))
+    ref = np.concatenate([_sdpa_bottom_right(Q[0:10], KV[0:10], 0.4, dv),
+                          _sdpa_bottom_right(Q[10:16], KV[10:25], 0.4, dv)])
+    _, idx, out, lse = oracle.forward_rows(q, k, w, Q, KV, cu_q, cu_kv, topk=S, scale=0.4, d_v=dv,
+                                           rows=range(T))
+    assert np.allclose(out, ref, rtol=1e-12, atol=1e-12)
+    # the selection of a second-sequence row is every candidate of its own sequence
+    assert list(idx[10][idx[10] >= 0]) == list(range(10))
+    full = np.full((T, S), -1, dtype=np.int64)
+    for r in range(T):
+        n = (r + 1) if r < 10 else (nkv[1] - nq[1] + (r - 10) + 1)
+        full[r, :n] = np.arange(n)
+    out2, lse2 = oracle.sparse_mla(Q, KV, full, cu_q, cu_kv, 0.4, dv)
+    assert np.allclose(out2, ref, rtol=1e-12, atol=1e-12)
+    assert np.allclose(lse2, lse, rtol=1e-13)
+    # and sparse_mla's lse is the library logsumexp of the second sequence's scores
+    z = 0.4 * torch.from_numpy(Q[15]) @ torch.from_numpy(KV[10:25]).T
+    assert np.allclose(lse2[15], torch.logsumexp(z, dim=1).numpy(), rtol=1e-13)
+
+
 def test_attention_lse_against_library_logsumexp():
     rng = np.random.default_rng(7)
     Q = rng.standard_normal((3, 10))
