@@ -191,14 +191,13 @@ def oracle_sample(wl, target_s, seed=0, threads=None):
     Returns (tokens/s extrapolated to the whole workload, description, seconds
     measured, threads used)."""
     import oracle
-    from threadpoolctl import threadpool_limits
     from tests.helpers import cu_np, idx_real, mla_real
 
     cu_q, cu_kv = cu_np(wl)
     _, pos, kv0, n = oracle.query_positions(cu_q, cu_kv)
     T = len(n)
     w_all = wl.w.float().cpu().numpy().astype(np.float64)
-    with threadpool_limits(limits=threads, user_api="blas"):
+    with _blas().limit(threads):
         used = blas_threads()
         # decode of the key rows is per sequence, timed once and charged in full
         t0 = time.perf_counter()
@@ -244,7 +243,74 @@ def cpu_baseline(wl, seconds):
             "host_cpus": os.cpu_count()}
 
 
+class _BlasThreads:
+    """Get / set the thread count of numpy's OpenBLAS: threadpoolctl when it is
+    installed, else the library's own entry points found through ctypes."""
+
+    def __init__(self):
+        self.get = self.set = None
+        try:
+            import threadpoolctl  # noqa: F401
+            self.kind = "threadpoolctl"
+            return
+        except Exception:
+            pass
+        import ctypes
+        import re
+        import numpy  # noqa: F401  (loads its BLAS)
+        try:
+            with open("/proc/self/maps") as f:
+                libs = sorted(set(re.findall(r"(/\S*openblas\S*\.so\S*)", f.read())))
+        except OSError:
+            libs = []
+        for path in libs:
+            h = ctypes.CDLL(path)
+            for pre in ("scipy_openblas_", "openblas_"):
+                for suf in ("64_", ""):
+                    g, st = f"{pre}get_num_threads{suf}", f"{pre}set_num_threads{suf}"
+                    if hasattr(h, g) and hasattr(h, st):
+                        self.get, self.set = getattr(h, g), getattr(h, st)
+                        self.get.restype = ctypes.c_int
+                        self.set.argtypes = [ctypes.c_int]
+                        self.kind = "openblas"
+                        return
+        self.kind = None
+
+    def limit(self, n):
+        """Context manager: at most n BLAS threads inside (None: unchanged)."""
+        import contextlib
+        if n is None or self.kind is None:
+            return contextlib.nullcontext()
+        if self.kind == "threadpoolctl":
+            from threadpoolctl import threadpool_limits
+            return threadpool_limits(limits=n, user_api="blas")
+        outer = self
+
+        class _Ctx:
+            def __enter__(self):
+                self.old = outer.get()
+                outer.set(int(n))
+
+            def __exit__(self, *exc):
+                outer.set(self.old)
+        return _Ctx()
+
+
+_BLAS = None
+
+
+def _blas():
+    global _BLAS
+    if _BLAS is None:
+        _BLAS = _BlasThreads()
+    return _BLAS
+
+
 def blas_threads():
+    """Threads numpy's BLAS uses now."""
+    b = _blas()
+    if b.kind == "openblas":
+        return int(b.get())
     try:
         from threadpoolctl import threadpool_info
         th = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
