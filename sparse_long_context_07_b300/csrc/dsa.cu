@@ -370,9 +370,14 @@ dsa_status_t launch_sparse_mla(const DeviceInfo& dev, const dsa_batch_t* b, cons
       return fail(DSA_ERROR_INSUFFICIENT_WORKSPACE, "sparse MLA needs %zu bytes of workspace, got %zu",
                   plan.ws_bytes, ws_bytes);
     if (ws && !aligned16(ws)) return fail(DSA_ERROR_INVALID_VALUE, "workspace must be 16-byte aligned");
-    CUtensorMap tm_q;
+    CUtensorMap tm_q, tm_out;
     DSA_TRY(encode_2d(&tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, m->q, dsa::mla_tc::kDqk,
                       static_cast<uint64_t>(b->total_q) * dsa::mla_tc::kHeads, dsa::mla_tc::kDqk * 2, 64,
+                      dsa::mla_tc::kHeads));
+    // the output rows of this launch, [rows x 128 heads, 512] bf16, stored in
+    // boxes of 64 columns x 128 heads
+    DSA_TRY(encode_2d(&tm_out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, out, dsa::mla_tc::kDv,
+                      static_cast<uint64_t>(rows) * dsa::mla_tc::kHeads, dsa::mla_tc::kDv * 2, 64,
                       dsa::mla_tc::kHeads));
     dsa::mla_tc::Params P{};
     P.q = static_cast<const __nv_bfloat16*>(m->q);
@@ -387,6 +392,9 @@ dsa_status_t launch_sparse_mla(const DeviceInfo& dev, const dsa_batch_t* b, cons
     P.row0 = r0;
     P.nsplit = plan.nsplit;
     P.tiles_per_split = plan.tiles_per_split;
+    P.units = rows * plan.nsplit;
+    // about one wave of clusters (two CTAs per SM pair) runs at a time
+    P.prefetch_ahead = std::max(1, dev.sms / 2);
     P.out = static_cast<__nv_bfloat16*>(out);
     P.lse = lse;
     if (plan.nsplit > 1) {
@@ -396,7 +404,7 @@ dsa_status_t launch_sparse_mla(const DeviceInfo& dev, const dsa_batch_t* b, cons
     }
     const int64_t ctas = 2 * rows * plan.nsplit;
     if (ctas > 2147483647ll) return fail(DSA_ERROR_NOT_SUPPORTED, "too many query rows in one call");
-    dsa::mla_tc::mla_kernel<<<static_cast<unsigned>(ctas), dsa::mla_tc::kThreads, dsa::mla_tc::kSmemBytes, s>>>(tm_q, P);
+    dsa::mla_tc::mla_kernel<<<static_cast<unsigned>(ctas), dsa::mla_tc::kThreads, dsa::mla_tc::kSmemBytes, s>>>(tm_q, tm_out, P);
     DSA_TRY(check_launch("mla_tc"));
     tr.after(DSA_KERNEL_MLA_TC);
     if (plan.nsplit > 1) {

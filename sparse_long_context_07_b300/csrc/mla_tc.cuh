@@ -118,10 +118,12 @@ constexpr int kOffMo = kOffX + 2 * kXBytes;        // own maxima of the last two
 constexpr int kOffL = kOffMo + 2 * kHeads * 4;     // partial sums of the two roles [2][128]
 constexpr int kOffBar = kOffL + 2 * kHeads * 4;
 constexpr int kNumBars = kVStages + kKStages + kVStages + 17;
+constexpr int kOutBox = kHeads * 128;   // one [128 heads x 64 columns] bf16 box of the output, 16 KiB
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;
 static_assert(kOffQ % 1024 == 0 && kOffP % 1024 == 0 && kOffX % 16 == 0, "operand alignment");
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+static_assert((kHalf / 64) * kOutBox <= kVStages * kVStageBytes, "output staging fits in ring V");
 
 struct Params {
   const __nv_bfloat16* q;    // [total_q, 128, 576]
@@ -136,6 +138,8 @@ struct Params {
   int64_t row0;
   int nsplit;                // clusters per query row
   int tiles_per_split;
+  int64_t units;             // (row, split) units of this launch
+  int64_t prefetch_ahead;    // >0: also prefetch the queries of unit + this into L2
   __nv_bfloat16* out;        // nsplit == 1: [rows, 128, 512], relative to row0
   float* lse;                // nsplit == 1: [rows, 128] or nullptr
   float* part_o;             // nsplit > 1: [rows * nsplit, 128, 512] fp32
@@ -182,7 +186,7 @@ __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    mla_kernel(const __grid_constant__ CUtensorMap tm_q, const Params P) {
+    mla_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_out, const Params P) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte aligned base, derived by pointer arithmetic on the shared array
   // so that accesses through it stay shared-memory instructions
@@ -240,6 +244,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   };
 
   if (threadIdx.x == 0) {
+    if (half == 0 && P.prefetch_ahead > 0) {
+      // this token's queries and index list into L2 ahead of their loads,
+      // and the queries of the token that will likely run next on this SM
+      // pair (a wave of the grid later)
+      if (nt > 0) prefetch_l2_bulk(P.q + row * kHeads * kDqk, kHeads * kDqk * 2);
+      if (nt > 0 && !P.dense && (P.k & 3) == 0) prefetch_l2_bulk(idx_row, P.k * 4);
+      const int64_t nu = unit + P.prefetch_ahead;
+      if (nu < P.units) prefetch_l2_bulk(P.q + (P.row0 + nu / P.nsplit) * kHeads * kDqk, kHeads * kDqk * 2);
+    }
     for (int s = 0; s < kVStages; ++s) {
       mbar_init(full(s), kGatherThreads);
       mbar_init(v_empty(s), 1);
@@ -263,6 +276,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     for (int b = 0; b < 2; ++b) mbar_arrive_expect_tx(x_full(b), kXBytes);
     fence_proxy_async_smem();
     tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_out);
   }
   if (warp == kMmaWarp) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
   tc_fence_before();
@@ -562,7 +576,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const float inv = lt > 0.f ? 1.f / lt : 0.f;
     const float lse_v = lt > 0.f ? (m_use + __log2f(lt)) * 0.6931471805599453f : -INFINITY;
     if (P.nsplit == 1) {
-      __nv_bfloat16* orow = P.out + (rrel * kHeads + h) * kDv + half * kHalf + 128 * sr;
+      // O / l in bf16 into the freed ring V as four [128 heads x 64 columns]
+      // boxes with the 128-byte swizzle (every copy and MMA of the tile loop
+      // has completed: P V of the last tile was waited for), then TMA stores
+      // of the CTA's 256 output columns
+      uint8_t* ob = smem + kOffV;
 #pragma unroll 1
       for (int c = 0; c < kHalf / 64; ++c) {
         uint32_t o[32];
@@ -571,6 +589,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int u = 0; u < 32; ++u) o[u] = 0u;
         }
+        const int col = 128 * sr + 32 * c;   // column within this CTA's half
+        uint8_t* rowp = ob + (col >> 6) * kOutBox + h * 128;
+        const int ch0 = (col & 63) >> 3;
 #pragma unroll
         for (int v = 0; v < 4; ++v) {
           uint4 pk4;
@@ -578,8 +599,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           pk4.y = pack_bf16(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv);
           pk4.z = pack_bf16(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv);
           pk4.w = pack_bf16(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv);
-          *reinterpret_cast<uint4*>(orow + 32 * c + 8 * v) = pk4;
+          *reinterpret_cast<uint4*>(rowp + (((ch0 + v) ^ (h & 7)) << 4)) = pk4;
         }
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(1, kSoftmaxThreads);
+      if (threadIdx.x == 0) {
+#pragma unroll
+        for (int b = 0; b < kHalf / 64; ++b)
+          tma_store_2d(&tm_out, half * kHalf + 64 * b, static_cast<int32_t>(rrel * kHeads), sbase + kOffV + b * kOutBox);
+        bulk_commit();
+        bulk_wait_read();   // the staging buffer is read before the CTA may exit
       }
       if (half == 0 && sr == 0 && P.lse) P.lse[rrel * kHeads + h] = lse_v;
     } else {
