@@ -651,19 +651,21 @@ dsa_status_t dsa_quantize_e4m3(const void* x, dsa_dtype_t x_dtype, int64_t group
   DeviceInfo* dev;
   DSA_TRY(device_info(&dev));
   const bool bf16 = x_dtype == DSA_DTYPE_BF16;
-  if (group_elems <= dsa::quant::kWarpGroupMax) {
-    const int64_t per_cta = dsa::quant::kThreads / 32;   // one warp per group
+  namespace q = dsa::quant;
+  if (group_elems <= q::kWarpGroupMax) {
+    const int64_t per_cta = q::kThreads / 32;   // one warp per group
     const int64_t ctas = (groups + per_cta - 1) / per_cta;
-    dsa::quant::quantize_warp_kernel<<<static_cast<unsigned>(ctas), dsa::quant::kThreads, 0, stream>>>(
-        x, bf16, groups, group_elems, codes, scales);
+    q::quantize_warp_kernel<<<static_cast<unsigned>(ctas), q::kThreads, 0, stream>>>(x, bf16, groups, group_elems,
+                                                                                    codes, scales);
   } else {
     // one CTA per group (groups < 2^31 was checked above)
-    if (bf16)
-      dsa::quant::quantize_cta_kernel<true><<<static_cast<unsigned>(groups), dsa::quant::CtaShape<true>::kThreads,
-                                              0, stream>>>(x, group_elems, codes, scales);
+    const unsigned grid = static_cast<unsigned>(groups);
+    if (!bf16)
+      q::quantize_cta_kernel<q::kF32x4><<<grid, 256, 0, stream>>>(x, group_elems, codes, scales);
+    else if (group_elems % 8 == 0)
+      q::quantize_cta_kernel<q::kBf16x8><<<grid, 256, 0, stream>>>(x, group_elems, codes, scales);
     else
-      dsa::quant::quantize_cta_kernel<false><<<static_cast<unsigned>(groups), dsa::quant::CtaShape<false>::kThreads,
-                                               0, stream>>>(x, group_elems, codes, scales);
+      q::quantize_cta_kernel<q::kBf16x4><<<grid, 256, 0, stream>>>(x, group_elems, codes, scales);
   }
   return check_launch("quantize_e4m3");
 }

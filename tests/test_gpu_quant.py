@@ -93,3 +93,31 @@ def test_quantize_argument_checks():
         dsa.quantize_e4m3(x[1:61], codes, scales, 4)     # x not 16-byte aligned
     assert e.value.status == dsa.ERROR_INVALID_VALUE
     dsa.quantize_e4m3(x[:0], codes, scales, 4)            # no groups: nothing to do
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("group_elems", [128, 8192, 1028])
+def test_quantize_rounding_midpoints_bit_exact(dtype, group_elems):
+    # quotients x / scale on, and one fp32 ulp either side of, every e4m3
+    # rounding midpoint (and on the codes themselves), for group scales of
+    # awkward mantissas: the division and the round-to-nearest-even must
+    # agree with the oracle's IEEE fp32 division and encoder bit for bit
+    v = oracle.decode_e4m3(np.arange(0x7F, dtype=np.uint8))          # finite non-negative codes, ascending
+    mid = ((v[1:] + v[:-1]) / 2).astype(np.float32)
+    t = np.concatenate([mid, np.nextafter(mid, np.float32(np.inf)), np.nextafter(mid, np.float32(-np.inf)),
+                        v.astype(np.float32)])
+    rng = np.random.default_rng(group_elems)
+    groups = []
+    for amax in (448.0 * 1.3, 448.0 * 0.7371, 3.1e-3, 7.77e4, 1.0, 448.0):
+        scale = np.float32(amax) / np.float32(448.0)
+        for _ in range(2):
+            tt = rng.permutation(np.resize(t, group_elems - 1))
+            x = (tt * scale).astype(np.float32)
+            x = np.minimum(np.abs(x), np.float32(amax)) * rng.choice([-1, 1], size=x.shape).astype(np.float32)
+            groups.append(np.concatenate([[np.float32(amax)], x]).astype(np.float32))
+    xg = torch.from_numpy(np.stack(groups)).to(dtype).cuda().contiguous()
+    codes, scales = _run(xg, group_elems)
+    ref_c, ref_s = _oracle(xg, group_elems)
+    assert np.array_equal(scales.view(np.uint32), ref_s.view(np.uint32))
+    bad = np.nonzero(codes != ref_c.reshape(-1))[0]
+    assert bad.size == 0, f"{bad.size} codes differ, first at {bad[:5]}"
