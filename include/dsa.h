@@ -241,6 +241,34 @@ dsa_status_t dsa_dense_mla(const dsa_batch_t* batch, const dsa_mla_t* mla, void*
 dsa_status_t dsa_quantize_e4m3(const void* x, dsa_dtype_t x_dtype, int64_t groups, int32_t group_elems,
                                uint8_t* codes, float* scales, cudaStream_t stream);
 
+/* The lightning indexer's dense warm-up loss and its gradient ("DeepSeek V3.2:
+ * How Far Can Open Models Go If You Actually Try?", §3.3, Stage 1:
+ * L_I = sum_t KL(p_t || softmax(I_t)); "DeepSeek-V3.2: Pushing the Frontier
+ * of Open Large Language Models", Modeling, Objective Functions: p_t is the
+ * main attention's dense scores aggregated over the heads, L1-normalised).
+ * For every query row t with candidates s = 0..p (the causal domain of the
+ * forward pass):
+ *   p_t[s] = (1/H) sum_h softmax_s(mla.scale * mla.q[t,h] . mla.kv[s]),
+ *   I_t    = the index scores of dsa_index_scores,
+ *   loss_rows[t] = sum_s p_t[s] (log p_t[s] - log softmax(I_t)_s), 0 log 0 = 0,
+ * and the gradients of sum_t loss_rows[t] with respect to the real-valued
+ * indexer inputs (code * scale for E4M3) and the head weights, ReLU'(0) = 0:
+ *   dq [total_q, n_heads, head_dim], dk [total_kv, head_dim], dw [total_q,
+ *   n_heads], all fp32 and overwritten (keys of no query row get 0).
+ * loss_rows [total_q] fp32.  The mla value columns are not read.  Arithmetic
+ * is fp32 on CUDA cores (the indexer scores use the forward kernels); the
+ * workspace holds (3 + n_heads) * round_up(max_seqlen_kv, 4) fp32 per query
+ * row of a chunk (dsa_indexer_loss_workspace_size: min_bytes = one row,
+ * preferred_bytes = every row at once, up to 65535 rows per chunk).  Same
+ * shape support as the forward's CUDA-core kernels (n_heads <= 64,
+ * head_dim <= 128; MLA d_qk <= 1024, BF16 or F32).  All pointers 16-byte
+ * aligned device memory; errors as dsa_forward. */
+dsa_status_t dsa_indexer_loss_workspace_size(const dsa_batch_t* batch, const dsa_indexer_t* indexer,
+                                             const dsa_mla_t* mla, size_t* min_bytes, size_t* preferred_bytes);
+dsa_status_t dsa_indexer_warmup_loss(const dsa_batch_t* batch, const dsa_indexer_t* indexer,
+                                     const dsa_mla_t* mla, float* loss_rows, float* dq, float* dk, float* dw,
+                                     void* ws, size_t ws_bytes, cudaStream_t stream);
+
 /* The whole forward pass: steps 1-3 for every query row, processed in query
  * chunks sized to ws_bytes.  out/lse as dsa_sparse_mla; idx_out (nullable)
  * [total_q, k] receives the selected positions as dsa_topk writes them. */

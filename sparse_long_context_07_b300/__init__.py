@@ -94,6 +94,9 @@ _sig = {
                                           _P, _P]),
     "dsa_forward_streamed": (ctypes.c_int, [_P, _P, _P, ctypes.c_int32, _P, _P, _P, _P, _P, _P,
                                             ctypes.c_size_t, _P, _P, _P]),
+    "dsa_indexer_loss_workspace_size": (ctypes.c_int, [_P, _P, _P, ctypes.POINTER(ctypes.c_size_t),
+                                                       ctypes.POINTER(ctypes.c_size_t)]),
+    "dsa_indexer_warmup_loss": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "dsa_read_device_errors": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_uint32)]),
     "dsa_debug_inject_fault": (None, [ctypes.c_uint32]),
 }
@@ -305,6 +308,22 @@ def forward(batch: Batch, indexer: Indexer, mla: Mla, k: int, out, lse=None, idx
         st = lib().dsa_forward_traced(_ref(batch), _ref(indexer), _ref(mla), int(k), _ptr(out), _ptr(lse),
                                      _ptr(idx_out), _ptr(ws), nbytes, _stream(stream), ctypes.byref(trace.c))
     _check(st, "dsa_forward")
+
+
+def indexer_loss_workspace_size(batch: Batch, indexer: Indexer, mla: Mla):
+    mn, pref = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    _check(lib().dsa_indexer_loss_workspace_size(_ref(batch), _ref(indexer), _ref(mla), ctypes.byref(mn),
+                                                 ctypes.byref(pref)), "dsa_indexer_loss_workspace_size")
+    return int(mn.value), int(pref.value)
+
+
+def indexer_warmup_loss(batch: Batch, indexer: Indexer, mla: Mla, loss_rows, dq, dk, dw, ws, stream=None):
+    """The indexer's dense warm-up loss per query row and its gradients with
+    respect to the real-valued indexer q, k and the head weights w
+    (dsa_indexer_warmup_loss); every output is fp32 and overwritten."""
+    nbytes = 0 if ws is None else ws.numel() * ws.element_size()
+    _check(lib().dsa_indexer_warmup_loss(_ref(batch), _ref(indexer), _ref(mla), _ptr(loss_rows), _ptr(dq), _ptr(dk),
+                                         _ptr(dw), _ptr(ws), nbytes, _stream(stream)), "dsa_indexer_warmup_loss")
 
 
 def _host_ptr(t) -> Optional[int]:

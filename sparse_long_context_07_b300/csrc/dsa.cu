@@ -17,6 +17,7 @@
 #include "dsa.h"
 #include "common.cuh"
 #include "indexer_tc.cuh"
+#include "kl.cuh"
 #include "mla_tc.cuh"
 #include "quant.cuh"
 #include "ptx.cuh"
@@ -499,6 +500,23 @@ dsa_status_t static_scratch_address(void** out) {
   return DSA_SUCCESS;
 }
 
+// ---------------------------------------------------------------------------
+// Indexer warm-up loss: workspace per query row of a chunk is the scores /
+// gradient row, the target row and its per-head scratch row, and the
+// H_I x ld matrix c[t, j, s] of the backward.
+size_t kl_row_bytes(const dsa_batch_t* b, const dsa_indexer_t* ix) {
+  const int64_t ld = round_up(std::max(1, b->max_seqlen_kv), 4);
+  return static_cast<size_t>((3 + ix->n_heads) * ld) * 4;
+}
+constexpr int64_t kKlMaxChunk = 65535;   // grid.y of the backward kernel
+
+dsa_status_t check_kl(const dsa_batch_t* batch, const dsa_indexer_t* ix, const dsa_mla_t* mla) {
+  DSA_TRY(check_batch(batch));
+  DSA_TRY(check_indexer(ix, batch));
+  DSA_TRY(check_mla(mla, batch));
+  return DSA_SUCCESS;
+}
+
 }  // namespace
 
 extern "C" {
@@ -668,6 +686,74 @@ dsa_status_t dsa_quantize_e4m3(const void* x, dsa_dtype_t x_dtype, int64_t group
       q::quantize_cta_kernel<q::kBf16x4><<<grid, 256, 0, stream>>>(x, group_elems, codes, scales);
   }
   return check_launch("quantize_e4m3");
+}
+
+dsa_status_t dsa_indexer_loss_workspace_size(const dsa_batch_t* batch, const dsa_indexer_t* indexer,
+                                             const dsa_mla_t* mla, size_t* min_bytes, size_t* preferred_bytes) {
+  DSA_TRY(check_kl(batch, indexer, mla));
+  const size_t per_row = kl_row_bytes(batch, indexer);
+  const size_t mn = batch->total_q > 0 ? per_row + 256 : 0;
+  const size_t pref = batch->total_q > 0 ? per_row * std::min<int64_t>(batch->total_q, kKlMaxChunk) + 256 : 0;
+  if (min_bytes) *min_bytes = mn;
+  if (preferred_bytes) *preferred_bytes = pref;
+  return DSA_SUCCESS;
+}
+
+dsa_status_t dsa_indexer_warmup_loss(const dsa_batch_t* batch, const dsa_indexer_t* indexer, const dsa_mla_t* mla,
+                                     float* loss_rows, float* dq, float* dk, float* dw, void* ws, size_t ws_bytes,
+                                     cudaStream_t stream) {
+  DSA_TRY(check_kl(batch, indexer, mla));
+  if (batch->total_q == 0) return DSA_SUCCESS;
+  if (!loss_rows || !dq || !dk || !dw || !aligned16(loss_rows) || !aligned16(dq) || !aligned16(dk) || !aligned16(dw))
+    return fail(DSA_ERROR_INVALID_VALUE, "loss_rows, dq, dk and dw must be non-NULL and 16-byte aligned");
+  if (!ws || !aligned16(ws)) return fail(DSA_ERROR_INVALID_VALUE, "workspace must be non-NULL and 16-byte aligned");
+  const size_t per_row = kl_row_bytes(batch, indexer);
+  if (ws_bytes < per_row + 256)
+    return fail(DSA_ERROR_INSUFFICIENT_WORKSPACE, "dsa_indexer_warmup_loss needs at least %zu bytes of workspace, got %zu",
+                per_row + 256, ws_bytes);
+  DeviceInfo* dev;
+  DSA_TRY(device_info(&dev));
+  const int64_t ld = round_up(std::max(1, batch->max_seqlen_kv), 4);
+  const int64_t chunk = std::min<int64_t>({batch->total_q, kKlMaxChunk, static_cast<int64_t>((ws_bytes - 256) / per_row)});
+  const int HI = indexer->n_heads, D = indexer->head_dim;
+  float* IG = static_cast<float*>(ws);
+  float* P = IG + chunk * ld;
+  float* Z = P + chunk * ld;
+  float* C = Z + chunk * ld;
+  if (cudaMemsetAsync(dk, 0, static_cast<size_t>(batch->total_kv) * D * 4, stream) != cudaSuccess ||
+      cudaMemsetAsync(dw, 0, static_cast<size_t>(batch->total_q) * HI * 4, stream) != cudaSuccess)
+    return fail(DSA_ERROR_LAUNCH, "clearing dk / dw failed: %s", cudaGetErrorString(cudaGetLastError()));
+  const int idtype = indexer->dtype, mdtype = mla->dtype;
+  Tracer tr{nullptr, stream};
+  for (int64_t r0 = 0; r0 < batch->total_q; r0 += chunk) {
+    const int64_t r1 = std::min<int64_t>(batch->total_q, r0 + chunk);
+    const unsigned rows = static_cast<unsigned>(r1 - r0);
+    // I[t, s] for the chunk (the forward indexer kernels)
+    DSA_TRY(launch_index_scores(*dev, batch, indexer, IG, ld, r0, r1, stream, tr));
+    dsa::kl::target_kernel<<<rows, dsa::kl::kThreads, 0, stream>>>(
+        mla->q, mla->kv, mdtype, mla->n_heads, mla->d_qk, mla->scale, batch->cu_seqlens_q, batch->cu_seqlens_kv,
+        batch->num_seqs, r0, P, Z, ld);
+    DSA_TRY(check_launch("kl_target"));
+    dsa::kl::loss_kernel<<<rows, dsa::kl::kThreads, 0, stream>>>(IG, P, ld, batch->cu_seqlens_q,
+                                                                 batch->cu_seqlens_kv, batch->num_seqs, r0, loss_rows);
+    DSA_TRY(check_launch("kl_loss"));
+    dim3 gx(static_cast<unsigned>((batch->max_seqlen_kv + dsa::kl::kBwdThreads - 1) / dsa::kl::kBwdThreads), rows);
+    dsa::kl::bwd_x_kernel<<<gx, dsa::kl::kBwdThreads, 0, stream>>>(
+        indexer->q, indexer->q_scale, indexer->k, indexer->k_scale, indexer->w, HI, D, idtype, IG, ld,
+        batch->cu_seqlens_q, batch->cu_seqlens_kv, batch->num_seqs, r0, C, dw);
+    DSA_TRY(check_launch("kl_bwd_x"));
+    dsa::kl::bwd_dq_kernel<<<rows, dsa::kl::kBwdThreads, 0, stream>>>(
+        C, indexer->k, indexer->k_scale, HI, D, idtype, ld, batch->cu_seqlens_q, batch->cu_seqlens_kv,
+        batch->num_seqs, r0, dq);
+    DSA_TRY(check_launch("kl_bwd_dq"));
+    if (batch->total_kv > 0) {
+      dsa::kl::bwd_dk_kernel<<<static_cast<unsigned>(batch->total_kv), dsa::kl::kBwdThreads, 0, stream>>>(
+          C, indexer->q, indexer->q_scale, HI, D, idtype, ld, batch->cu_seqlens_q, batch->cu_seqlens_kv,
+          batch->num_seqs, r0, r1, dk);
+      DSA_TRY(check_launch("kl_bwd_dk"));
+    }
+  }
+  return DSA_SUCCESS;
 }
 
 dsa_status_t dsa_forward_traced(const dsa_batch_t* batch, const dsa_indexer_t* indexer, const dsa_mla_t* mla,
