@@ -138,7 +138,8 @@ enum {
   DSA_KERNEL_TOPK = 3,
   DSA_KERNEL_MLA_TC = 4,
   DSA_KERNEL_MLA_SIMT = 5,
-  DSA_KERNEL_MLA_COMBINE = 6
+  DSA_KERNEL_MLA_COMBINE = 6,
+  DSA_KERNEL_HIST_CLEAR = 7  /* zeroing of the first-digit histograms (dsa_index_scores_hist) */
 };
 typedef struct {
   int32_t capacity; /* number of events[] (kernel_ids[] holds capacity-1) */
@@ -170,6 +171,24 @@ dsa_status_t dsa_index_scores(const dsa_batch_t* batch, const dsa_indexer_t* ind
  * (-inf in the -1 slots).  1 <= k <= 16384. */
 dsa_status_t dsa_topk(const dsa_batch_t* batch, const float* scores, int64_t ld_scores,
                       int32_t k, int32_t* idx, float* vals, cudaStream_t stream);
+
+/* Steps 1 and 2 with the selection's first pass fused into the indexer (no
+ * counterpart on the pages beyond their separate indexer and "Top-k
+ * operation" modules): dsa_index_scores_hist writes the scores exactly as
+ * dsa_index_scores does and also, for every query row, the histogram of the
+ * first radix digit of its scores (hist [total_q, 2048] uint32: bin = top 11
+ * bits of the order-preserving 32-bit key of the fp32 score, -0 counted as
+ * +0; the call clears hist first).  dsa_topk_hist then selects exactly as
+ * dsa_topk does (same result, bit for bit) without re-reading a row for that
+ * histogram.  Tensor-core indexer instance only (E4M3, 64 heads x 128), else
+ * DSA_ERROR_NOT_SUPPORTED.  On one B300 and the 131072-token prefill the
+ * histograms cost the indexer more time (+6 ms) than they save in the
+ * selection (-4 ms), so dsa_forward runs the unfused pair; the fused pair
+ * reads each score row once instead of twice. */
+dsa_status_t dsa_index_scores_hist(const dsa_batch_t* batch, const dsa_indexer_t* indexer,
+                                   float* scores, int64_t ld_scores, uint32_t* hist, cudaStream_t stream);
+dsa_status_t dsa_topk_hist(const dsa_batch_t* batch, const float* scores, int64_t ld_scores,
+                           const uint32_t* hist, int32_t k, int32_t* idx, float* vals, cudaStream_t stream);
 
 /* Step 3 alone.  For every query row r: softmax attention of its n_heads
  * queries over the latent rows idx[r * k + i] (sequence-local positions; -1

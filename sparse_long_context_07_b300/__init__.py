@@ -34,7 +34,7 @@ ERROR_BAD_INDEX = 7
 DTYPE_F32, DTYPE_BF16, DTYPE_E4M3 = 0, 1, 2
 DEVERR_TIMEOUT, DEVERR_BAD_INDEX = 0x1, 0x2
 KERNEL_NAMES = {1: "indexer_tc", 2: "indexer_simt", 3: "topk", 4: "mla_tc", 5: "mla_simt",
-                6: "mla_combine"}
+                6: "mla_combine", 7: "hist_clear"}
 
 
 class DSAError(RuntimeError):
@@ -87,6 +87,8 @@ _sig = {
     "dsa_dense_mla": (ctypes.c_int, [_P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "dsa_quantize_e4m3": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_int64, ctypes.c_int32, _P, _P, _P]),
     "dsa_topk": (ctypes.c_int, [_P, _P, ctypes.c_int64, ctypes.c_int32, _P, _P, _P]),
+    "dsa_index_scores_hist": (ctypes.c_int, [_P, _P, _P, ctypes.c_int64, _P, _P]),
+    "dsa_topk_hist": (ctypes.c_int, [_P, _P, ctypes.c_int64, _P, ctypes.c_int32, _P, _P, _P]),
     "dsa_sparse_mla": (ctypes.c_int, [_P, _P, _P, ctypes.c_int32, _P, _P, _P, ctypes.c_size_t, _P]),
     "dsa_sparse_mla_noalloc": (ctypes.c_int, [_P, _P, _P, ctypes.c_int32, _P, _P, _P]),
     "dsa_forward": (ctypes.c_int, [_P, _P, _P, ctypes.c_int32, _P, _P, _P, _P, ctypes.c_size_t, _P]),
@@ -225,6 +227,19 @@ def index_scores(batch: Batch, indexer: Indexer, scores, ld: int, stream=None):
 def topk(batch: Batch, scores, ld: int, k: int, idx, vals=None, stream=None):
     _check(lib().dsa_topk(_ref(batch), _ptr(scores), int(ld), int(k), _ptr(idx), _ptr(vals),
                          _stream(stream)), "dsa_topk")
+
+
+def index_scores_hist(batch: Batch, indexer: Indexer, scores, ld: int, hist, stream=None):
+    """dsa_index_scores plus each row's first-digit histogram (hist: int32 or
+    uint32 [total_q, 2048], cleared by the call)."""
+    _check(lib().dsa_index_scores_hist(_ref(batch), _ref(indexer), _ptr(scores), int(ld), _ptr(hist),
+                                       _stream(stream)), "dsa_index_scores_hist")
+
+
+def topk_hist(batch: Batch, scores, ld: int, hist, k: int, idx, vals=None, stream=None):
+    """dsa_topk taking the rows' first-digit histograms from index_scores_hist."""
+    _check(lib().dsa_topk_hist(_ref(batch), _ptr(scores), int(ld), _ptr(hist), int(k), _ptr(idx), _ptr(vals),
+                               _stream(stream)), "dsa_topk_hist")
 
 
 def sparse_mla(batch: Batch, mla: Mla, idx, k: int, out, lse=None, ws=None, stream=None):

@@ -36,6 +36,18 @@ __device__ __forceinline__ RowGeom row_geom(const int32_t* __restrict__ cu_q,
   return g;
 }
 
+// Monotone map of an fp32 score to a 32-bit key (larger score, larger key);
+// -0 maps like +0.  Selection works on these keys; the top kRadixBits bits
+// are the first radix digit (histogram bin) of a score.
+__device__ __forceinline__ uint32_t order_key(float x) {
+  uint32_t b = __float_as_uint(x);
+  b = (b == 0x80000000u) ? 0u : b;
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+constexpr int kRadixBits = 11;
+constexpr int kRadixBins = 1 << kRadixBits;          // 2048 bins of the first digit
+constexpr int kRadixShift = 32 - kRadixBits;         // bin = order_key >> 21
+
 // Block-wide inclusive scan (ascending thread order) of one value per thread.
 // `warp_sums` is shared scratch of 32 words.  Every thread must call it.
 template <int kThreads>

@@ -92,7 +92,9 @@ dsa_status_t device_info(DeviceInfo** out) {
   if (!d.ok) return fail(DSA_ERROR_DEVICE, "device %d is not an sm_103 (B300) GPU", dev);
   if (!g_encode) return fail(DSA_ERROR_DEVICE, "cuTensorMapEncodeTiled unavailable");
   if (!d.attrs_set) {
-    if (cudaFuncSetAttribute(dsa::idx_tc::indexer_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(dsa::idx_tc::indexer_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             dsa::idx_tc::kSmemBytes) != cudaSuccess ||
+        cudaFuncSetAttribute(dsa::idx_tc::indexer_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              dsa::idx_tc::kSmemBytes) != cudaSuccess ||
         cudaFuncSetAttribute(dsa::mla_tc::mla_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              dsa::mla_tc::kSmemBytes) != cudaSuccess ||
@@ -224,9 +226,11 @@ dsa_status_t check_k(int32_t k) {
 // Per-step launchers over query rows [r0, r1).  Output/intermediate pointers
 // (scores, idx, vals, out, lse) already point at row r0.
 // ---------------------------------------------------------------------------
+// hist (optional, tensor-core indexer only): [r1 - r0][2048] zeroed first-digit
+// histograms that the indexer fills for the top-k.
 dsa_status_t launch_index_scores(const DeviceInfo& dev, const dsa_batch_t* b, const dsa_indexer_t* ix,
                                  float* scores, int64_t ld, int64_t r0, int64_t r1, cudaStream_t s,
-                                 Tracer& tr) {
+                                 Tracer& tr, uint32_t* hist = nullptr) {
   const int64_t rows = r1 - r0;
   if (rows <= 0) return DSA_SUCCESS;
   if (indexer_is_tc(ix)) {
@@ -243,6 +247,7 @@ dsa_status_t launch_index_scores(const DeviceInfo& dev, const dsa_batch_t* b, co
     P.w = ix->w;
     P.scores = scores;
     P.ld = ld;
+    P.hist = hist;
     P.cu_q = b->cu_seqlens_q;
     P.cu_kv = b->cu_seqlens_kv;
     P.num_seqs = b->num_seqs;
@@ -262,14 +267,17 @@ dsa_status_t launch_index_scores(const DeviceInfo& dev, const dsa_batch_t* b, co
       P.max_tiles = 1 << 24;
     }
     const int grid = dev.sms;
-    dsa::idx_tc::indexer_kernel<<<grid, dsa::idx_tc::kThreads, dsa::idx_tc::kSmemBytes, s>>>(tm_q, tm_k, P);
+    if (hist)
+      dsa::idx_tc::indexer_kernel<true><<<grid, dsa::idx_tc::kThreads, dsa::idx_tc::kSmemBytes, s>>>(tm_q, tm_k, P);
+    else
+      dsa::idx_tc::indexer_kernel<false><<<grid, dsa::idx_tc::kThreads, dsa::idx_tc::kSmemBytes, s>>>(tm_q, tm_k, P);
     DSA_TRY(check_launch("indexer_tc"));
     tr.after(DSA_KERNEL_INDEXER_TC);
   } else {
     if (rows > 65535) {
       for (int64_t c = r0; c < r1; c += 65535) {
         const int64_t e = std::min<int64_t>(r1, c + 65535);
-        DSA_TRY(launch_index_scores(dev, b, ix, scores + (c - r0) * ld, ld, c, e, s, tr));
+        DSA_TRY(launch_index_scores(dev, b, ix, scores + (c - r0) * ld, ld, c, e, s, tr, nullptr));
       }
       return DSA_SUCCESS;
     }
@@ -286,13 +294,14 @@ dsa_status_t launch_index_scores(const DeviceInfo& dev, const dsa_batch_t* b, co
 
 // A few rows (a decode batch) cannot fill the device one CTA per row: each
 // row then gets a cluster of CTAs, each taking a slice of the row.
+// hist (optional): the rows' first-digit histograms from the indexer.
 dsa_status_t launch_topk(const DeviceInfo& dev, const dsa_batch_t* b, const float* scores, int64_t ld,
                          int32_t k, int32_t* idx, float* vals, int64_t r0, int64_t r1, cudaStream_t s,
-                         Tracer& tr) {
+                         Tracer& tr, const uint32_t* hist = nullptr) {
   if (r1 > r0 && (r1 - r0) * dsa::topk::kCluster <= 4 * static_cast<int64_t>(dev.sms)) {
     dsa::topk::topk_cluster_kernel<<<static_cast<unsigned>((r1 - r0) * dsa::topk::kCluster),
                                      dsa::topk::kCThreads, dsa::topk::kCSmemBytes, s>>>(
-        scores, ld, k, idx, vals, b->cu_seqlens_q, b->cu_seqlens_kv, b->num_seqs, r0);
+        scores, ld, k, idx, vals, b->cu_seqlens_q, b->cu_seqlens_kv, b->num_seqs, r0, hist);
     DSA_TRY(check_launch("topk_cluster"));
     tr.after(DSA_KERNEL_TOPK);
     return DSA_SUCCESS;
@@ -301,7 +310,7 @@ dsa_status_t launch_topk(const DeviceInfo& dev, const dsa_batch_t* b, const floa
     const int64_t e = std::min<int64_t>(r1, c + 2147483647ll);
     dsa::topk::topk_kernel<<<static_cast<unsigned>(e - c), dsa::topk::kThreads, dsa::topk::kSmemBytes, s>>>(
         scores + (c - r0) * ld, ld, k, idx + (c - r0) * k, vals ? vals + (c - r0) * k : nullptr,
-        b->cu_seqlens_q, b->cu_seqlens_kv, b->num_seqs, c);
+        b->cu_seqlens_q, b->cu_seqlens_kv, b->num_seqs, c, hist ? hist + (c - r0) * dsa::kRadixBins : nullptr);
     DSA_TRY(check_launch("topk"));
     tr.after(DSA_KERNEL_TOPK);
   }
@@ -430,6 +439,16 @@ dsa_status_t launch_sparse_mla(const DeviceInfo& dev, const dsa_batch_t* b, cons
 }
 
 int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+
+// Zero the first-digit histograms of `rows` query rows before the indexer
+// adds to them (nothing to do without a histogram buffer).
+dsa_status_t clear_hist(uint32_t* hist, int64_t rows, cudaStream_t s, Tracer& tr) {
+  if (!hist || rows <= 0) return DSA_SUCCESS;
+  if (cudaMemsetAsync(hist, 0, static_cast<size_t>(rows) * dsa::kRadixBins * 4, s) != cudaSuccess)
+    return fail(DSA_ERROR_LAUNCH, "clearing the top-k histograms failed: %s", cudaGetErrorString(cudaGetLastError()));
+  tr.after(DSA_KERNEL_HIST_CLEAR);
+  return DSA_SUCCESS;
+}
 
 // Forward workspace: [scores chunk | idx chunk | MLA split scratch]
 struct FwdPlan {
@@ -587,6 +606,40 @@ dsa_status_t dsa_topk(const dsa_batch_t* batch, const float* scores, int64_t ld_
   DSA_TRY(device_info(&dev));
   Tracer tr{nullptr, stream};
   return launch_topk(*dev, batch, scores, ld_scores, k, idx, vals, 0, batch->total_q, stream, tr);
+}
+
+dsa_status_t dsa_index_scores_hist(const dsa_batch_t* batch, const dsa_indexer_t* indexer, float* scores,
+                                   int64_t ld_scores, uint32_t* hist, cudaStream_t stream) {
+  DSA_TRY(check_batch(batch));
+  DSA_TRY(check_indexer(indexer, batch));
+  if (!indexer_is_tc(indexer))
+    return fail(DSA_ERROR_NOT_SUPPORTED, "dsa_index_scores_hist needs the tensor-core indexer (E4M3, 64 heads x 128)");
+  if (batch->total_q == 0) return DSA_SUCCESS;
+  if (!scores || !aligned16(scores) || !hist || !aligned16(hist))
+    return fail(DSA_ERROR_INVALID_VALUE, "scores and hist must be non-NULL and 16-byte aligned");
+  if (ld_scores < batch->max_seqlen_kv || ld_scores % 4 != 0)
+    return fail(DSA_ERROR_INVALID_VALUE, "ld_scores must be >= max_seqlen_kv and a multiple of 4");
+  DeviceInfo* dev;
+  DSA_TRY(device_info(&dev));
+  Tracer tr{nullptr, stream};
+  DSA_TRY(clear_hist(hist, batch->total_q, stream, tr));
+  return launch_index_scores(*dev, batch, indexer, scores, ld_scores, 0, batch->total_q, stream, tr, hist);
+}
+
+dsa_status_t dsa_topk_hist(const dsa_batch_t* batch, const float* scores, int64_t ld_scores, const uint32_t* hist,
+                           int32_t k, int32_t* idx, float* vals, cudaStream_t stream) {
+  DSA_TRY(check_batch(batch));
+  DSA_TRY(check_k(k));
+  if (batch->total_q == 0) return DSA_SUCCESS;
+  if (!scores || !aligned16(scores) || !idx || !aligned16(idx) || (vals && !aligned16(vals)) || !hist ||
+      !aligned16(hist))
+    return fail(DSA_ERROR_INVALID_VALUE, "scores, hist and idx must be non-NULL and 16-byte aligned");
+  if (ld_scores < batch->max_seqlen_kv || ld_scores % 4 != 0)
+    return fail(DSA_ERROR_INVALID_VALUE, "ld_scores must be >= max_seqlen_kv and a multiple of 4");
+  DeviceInfo* dev;
+  DSA_TRY(device_info(&dev));
+  Tracer tr{nullptr, stream};
+  return launch_topk(*dev, batch, scores, ld_scores, k, idx, vals, 0, batch->total_q, stream, tr, hist);
 }
 
 dsa_status_t dsa_sparse_mla(const dsa_batch_t* batch, const dsa_mla_t* mla, const int32_t* idx, int32_t k,

@@ -55,8 +55,9 @@ constexpr int kTmemCols = 512;
 constexpr int kOffK = 0;
 constexpr int kOffQ = kOffK + kStages * kTileBytes;
 constexpr int kOffW = kOffQ + 2 * kQBytes;
-constexpr int kOffBar = kOffW + 2 * kMaxTokens * kHeads * 4;
-constexpr int kNumBars = 2 * kStages + 2 + 2 + 2 + 2 + 1 + 2 * kEpiGroups;
+constexpr int kOffH = kOffW + 2 * kMaxTokens * kHeads * 4;    // first-digit histograms of an item's rows
+constexpr int kOffBar = kOffH + kMaxTokens * kRadixBins * 4;
+constexpr int kNumBars = 2 * kStages + 2 + 2 + 2 + 2 + 1 + 2 * kEpiGroups + 2;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
 
@@ -66,6 +67,8 @@ struct Params {
   const float* w;
   float* scores;
   int64_t ld;
+  uint32_t* hist;              // optional [rows of the launch][2048]: adds the first radix digit
+                               // histogram of every row's scores (zero on entry)
   const int32_t* cu_q;
   const int32_t* cu_kv;
   int num_seqs;
@@ -155,6 +158,9 @@ __device__ __forceinline__ void reduce_chunk(const uint32_t (&x)[32], const floa
   }
 }
 
+// kHist: also build the first radix digit histograms of the rows' scores
+// into P.hist (the forward runs without them; see dsa_index_scores_hist).
+template <bool kHist>
 __global__ void __launch_bounds__(kThreads, 1)
     indexer_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const Params P) {
@@ -174,6 +180,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t drain_bar = bar0 + 8u * (2 * kStages + 8);
   // w_full(e, b): warpgroup e has staged the head weights of its item with parity b
   auto w_full = [&](int e, int b) { return bar0 + 8u * (2 * kStages + 9 + 2 * e + b); };
+  // the item's histograms are cleared (h_zeroed) / complete (h_done): all
+  // epilogue threads arrive once per item
+  const uint32_t h_zeroed = bar0 + 8u * (2 * kStages + 9 + 2 * kEpiGroups);
+  const uint32_t h_done = h_zeroed + 8u;
+  uint32_t* hist_s = reinterpret_cast<uint32_t*>(smem + kOffH);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
 
@@ -189,6 +200,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(drain_bar, 1);
     for (int b = 0; b < 2 * kEpiGroups; ++b) mbar_init(w_full(b >> 1, b & 1), 128);
+    mbar_init(h_zeroed, kEpiGroups * 128);
+    mbar_init(h_done, kEpiGroups * 128);
     *abort_flag = 0;
     fence_mbar_init();
     fence_proxy_async_smem();
@@ -299,6 +312,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     Item item;
     int qi = 0, si = 0;
     bool ok = true;
+    // after the item's last tile: wait until every epilogue thread has added
+    // its scores, then add this thread's share of the histograms to the rows'
+    // global histograms (other CTAs may hold other key ranges of the rows)
+    auto flush_hist = [&](int hq) {
+      mbar_arrive(h_done);
+      if (!warp_wait(h_done, hq & 1, abort_flag)) { ok = false; return; }
+      const int ht = threadIdx.x - 128;
+      for (int i = ht; i < item.g * kRadixBins; i += kEpiGroups * 128) {
+        const uint32_t c = hist_s[i];
+        if (c) atomicAdd(P.hist + (item.t0 - P.row_begin + i / kRadixBins) * kRadixBins + (i % kRadixBins), c);
+      }
+    };
     for (int64_t it = blockIdx.x; ok && wk.seek(it, P, item); it += gridDim.x) {
       if (item.kt0 >= item.kt1) continue;
       // column group e of a slot: key tile u = e / g of the slot, token e % g
@@ -314,6 +339,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       mbar_arrive(w_full(e, qi & 1));
       if (!warp_wait(w_full(e, qi & 1), (qi >> 1) & 1, abort_flag)) break;
+      // this thread's share of the item's row histograms starts at zero (it
+      // flushed the same share at the end of its previous item)
+      const int ht = threadIdx.x - 128;                   // 0 .. 511
+      if (kHist) {
+        for (int i = ht; i < item.g * kRadixBins; i += kEpiGroups * 128) hist_s[i] = 0u;
+        mbar_arrive(h_zeroed);
+        if (!warp_wait(h_zeroed, qi & 1, abort_flag)) break;
+      }
+      const int hq = qi;
       ++qi;
       const int64_t srow = item.t0 + te - P.row_begin;   // score row of this token
       const int plim = item.pos0 + te;                    // its last candidate
@@ -344,8 +378,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           reduce_chunk(xa, wsm, acc);
           reduce_chunk(xb, wsm + 32, acc);
           const float2 tt = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
-          if (s <= plim) P.scores[srow * P.ld + s] = (tt.x + tt.y) * ks;
+          if (s <= plim) {
+            const float v = (tt.x + tt.y) * ks;
+            P.scores[srow * P.ld + s] = v;
+            if (kHist) atomicAdd(hist_s + te * kRadixBins + (order_key(v) >> kRadixShift), 1u);
+          }
         }
+        if (ok && kHist) flush_hist(hq);
         continue;
       }
       for (int kt0 = item.kt0; kt0 < item.kt1; kt0 += per, ++si) {
@@ -374,8 +413,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         reduce_chunk(xa, wsm, acc);
         reduce_chunk(xb, wsm + 32, acc);
         const float2 tt = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
-        if (s <= plim) P.scores[srow * P.ld + s] = (tt.x + tt.y) * ks;
+        if (s <= plim) {
+          const float v = (tt.x + tt.y) * ks;
+          P.scores[srow * P.ld + s] = v;
+          if (kHist) atomicAdd(hist_s + te * kRadixBins + (order_key(v) >> kRadixShift), 1u);
+        }
       }
+      if (ok && kHist) flush_hist(hq);
     }
   }
 

@@ -32,7 +32,7 @@ namespace dsa {
 namespace topk {
 
 constexpr int kThreads = 512;
-constexpr int kBins = 2048;     // histogram bins (11-bit digits)
+constexpr int kBins = kRadixBins;   // histogram bins (11-bit digits)
 constexpr int kPerThread = 8;   // elements per thread per compaction chunk
 constexpr int kMaxFastN = 131072;                 // positions covered by the bitmaps
 constexpr int kBitmapWords = kMaxFastN / 32;
@@ -50,12 +50,6 @@ struct Smem {
 };
 constexpr int kSmemBytes = static_cast<int>(sizeof(Smem));
 
-// Monotone map float -> uint32 (larger float, larger key); -0 maps like +0.
-__device__ __forceinline__ uint32_t order_key(float x) {
-  uint32_t b = __float_as_uint(x);
-  b = (b == 0x80000000u) ? 0u : b;
-  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-}
 
 // The digit (bin index) holding the kr-th largest key of `hist` (nbins bins,
 // thread t owns bins [4t, 4t+4)), and the number of keys in higher bins.
@@ -169,7 +163,7 @@ __device__ void select_general(const float* __restrict__ row, int n, int k, int3
 __global__ void __launch_bounds__(kThreads) topk_kernel(
     const float* __restrict__ scores, int64_t ld, int k, int32_t* __restrict__ idx,
     float* __restrict__ vals, const int32_t* __restrict__ cu_q, const int32_t* __restrict__ cu_kv,
-    int num_seqs, int64_t row0) {
+    int num_seqs, int64_t row0, const uint32_t* __restrict__ hist_in) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
 
@@ -190,13 +184,19 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(
     return;
   }
 
+  const int n4 = n >> 2;
+  const float4* __restrict__ row4 = reinterpret_cast<const float4*>(row);
+  int i4 = tid;
+  if (hist_in) {
+    // the indexer built this row's histogram of the top 11 key bits
+    const uint32_t* h = hist_in + (r - row0) * kBins;
+    for (int i = tid; i < kBins; i += kThreads) sm.hist[i] = __ldg(h + i);
+    __syncthreads();
+  } else {
   // ---- pass 1: histogram of the top 11 key bits
   for (int i = tid; i < kBins; i += kThreads) sm.hist[i] = 0;
   __syncthreads();
-  const int n4 = n >> 2;
-  const float4* __restrict__ row4 = reinterpret_cast<const float4*>(row);
   // four 16-byte loads in flight per thread
-  int i4 = tid;
   for (; i4 + 3 * kThreads < n4; i4 += 4 * kThreads) {
     float4 v[4];
 #pragma unroll
@@ -218,6 +218,7 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(
   }
   for (int i = 4 * n4 + tid; i < n; i += kThreads) atomicAdd(&sm.hist[order_key(__ldg(row + i)) >> 21], 1u);
   __syncthreads();
+  }
   find_digit(sm.hist, kBins, static_cast<uint32_t>(k), sm);
   const uint32_t bstar = sm.s_digit;
   const uint32_t kr = static_cast<uint32_t>(k) - sm.s_above;   // keys to take from bin b*
@@ -399,7 +400,7 @@ __device__ __forceinline__ void find_digit_c(const uint32_t* hist, int nbins, ui
 __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kCThreads) topk_cluster_kernel(
     const float* __restrict__ scores, int64_t ld, int k, int32_t* __restrict__ idx,
     float* __restrict__ vals, const int32_t* __restrict__ cu_q, const int32_t* __restrict__ cu_kv,
-    int num_seqs, int64_t row0) {
+    int num_seqs, int64_t row0, const uint32_t* __restrict__ hist_in) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   CSmem& sm = *reinterpret_cast<CSmem*>(smem_raw);
 
@@ -455,6 +456,14 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kCThreads) to
   for (int pass = 0; pass < 3; ++pass) {
     const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
     const uint32_t dmask = pass == 2 ? 0x3FFu : 0x7FFu;
+    if (pass == 0 && hist_in) {
+      // the indexer built the row's histogram of the top 11 key bits (the
+      // choice is uniform per cluster, so no cluster barrier is skipped by
+      // only some of its CTAs)
+      const uint32_t* h = hist_in + rl * kBins;
+      for (int i = tid; i < kBins; i += kCThreads) sm.ghist[i] = __ldg(h + i);
+      __syncthreads();
+    } else {
     for (int i = tid; i < kBins; i += kCThreads) sm.hist[i] = 0u;
     __syncthreads();
     for (int i = tid; i < len; i += kCThreads) {
@@ -472,6 +481,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kCThreads) to
       for (int q = 0; q < kCluster; ++q) st_cluster_u32(mapa_shared(ghist_base + 4u * b, q), v);
     }
     cluster_sync();   // every CTA holds the row histogram; the local ones may be reused
+    }
     find_digit_c(sm.ghist, pass == 2 ? 1024 : kBins, kr, sm);
     kr -= sm.s_above;
     prefix |= sm.s_digit << shift;
