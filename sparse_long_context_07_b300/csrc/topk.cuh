@@ -292,11 +292,13 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(
   }
   __syncthreads();
 
-  // ---- ordered emission: thread t scans bitmap words [8t, 8t+8)
-  const int w0 = tid * kWordsPerThread;
+  // ---- ordered emission: thread t scans bitmap words [wpt t, wpt t + wpt),
+  // the row's words spread over all threads
+  const int wpt = (nwords + kThreads - 1) / kThreads;   // at most kWordsPerThread
+  const int w0 = tid * wpt;
   uint32_t sel_cnt = 0, tie_cnt = 0;
-#pragma unroll
-  for (int q = 0; q < kWordsPerThread; ++q) {
+#pragma unroll 1
+  for (int q = 0; q < wpt; ++q) {
     if (w0 + q < nwords) {
       sel_cnt += __popc(sm.sel[w0 + q]);
       tie_cnt += __popc(sm.tie[w0 + q]);
@@ -308,7 +310,7 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(
   const uint32_t out_cnt = sel_cnt + take;
   uint32_t pos = block_inclusive_scan<kThreads>(out_cnt, sm.warp_sums, tot) - out_cnt;
 #pragma unroll 1
-  for (int q = 0; q < kWordsPerThread; ++q) {
+  for (int q = 0; q < wpt; ++q) {
     const int w = w0 + q;
     if (w >= nwords) break;
     uint32_t bits = sm.sel[w];
