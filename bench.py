@@ -556,13 +556,16 @@ def decode_rooflines(decode):
     """The ragged 128K decode's HBM-bound kernels as roofline entries."""
     out = []
     pk, src = _peaks()
-    for key, kernel in (("mla_hbm", "mla_tc+combine (decode)"), ("indexer_hbm", "indexer_tc (decode)")):
+    traffic_tab = load_traffic()
+    for key, kernel, tk in (("mla_hbm", "mla_tc+combine (decode)", "mla_tc"),
+                            ("indexer_hbm", "indexer_tc (decode)", "indexer_tc")):
         d = decode.get(key)
         if not d:
             continue
         ms = d["ms"]
         out.append(_entry(kernel, "hbm", "GB/s", d["bytes"], ms / 1e3, pk, "hbm", src,
-                          {"ms_per_step": ms, "workload": decode["workload"], "l2": "flushed before every step"}))
+                          {"ms_per_step": ms, "workload": decode["workload"], "l2": "flushed before every step",
+                           "traffic": traffic_tab.get(tk, {}).get(decode["workload"])}))
     q = decode.get("quantize")
     if q:
         out.append(_entry("quantize_e4m3", "hbm", "GB/s", q["bytes"], q["ms"] / 1e3, pk, "hbm", src,

@@ -16,6 +16,7 @@ Workloads (sizes and value distributions of the 128K-context DSA workloads):
   ragged128k  64 decode sequences, context ~ U[16384, 131072], 10% of
               each sequence's keys planted toward its query             (seed 4)
   prefill128k one 131072-token causal prefill                            (seed 5)
+  prefill128k_tail, prefill128k_mid, ragged128k_16: profiling-size cases
 All but ``tiny`` use the production dimensions: indexer 64 heads x 128 in
 e4m3 with per-token fp32 scales and w ~ N(0, 1/64); MLA-MQA 128 heads,
 d_qk = 576 (512 latent + 64 rope), d_v = 512, bf16, scale 192^-0.5, top-k 2048.
@@ -267,6 +268,27 @@ def prefill128k(device="cpu"):
     return make_workload("prefill128k", [131072], [131072], seed=5, device=device)
 
 
+def prefill128k_tail(device="cpu"):
+    """The last 2048 queries of a 131072-token causal prefill (the whole
+    131072-key cache, larger than L2): a profiling case shaped like the late
+    query chunks of prefill128k with a few GB on the device."""
+    return make_workload("prefill128k_tail", [2048], [131072], seed=5, device=device)
+
+
+def prefill128k_mid(device="cpu"):
+    """The last 2048 queries of a 65536-token causal prefill: shaped like the
+    middle query chunks of prefill128k (a 75 MB latent cache in play), with a
+    few GB on the device; a profiling case."""
+    return make_workload("prefill128k_mid", [2048], [65536], seed=5, device=device)
+
+
+def ragged128k_16(device="cpu"):
+    """The first 16 sequences of ragged128k (same lengths, planted keys): a
+    profiling-size decode case."""
+    lens = ragged_lengths(64, 16384, 131072, seed=4)[:16]
+    return make_workload("ragged128k_16", [1] * 16, lens, seed=4, planted=0.10, device=device)
+
+
 WORKLOADS = {
     "tiny": tiny,
     "decode8k": decode8k,
@@ -274,4 +296,7 @@ WORKLOADS = {
     "prefill32k": prefill32k,
     "ragged128k": ragged128k,
     "prefill128k": prefill128k,
+    "prefill128k_tail": prefill128k_tail,
+    "prefill128k_mid": prefill128k_mid,
+    "ragged128k_16": ragged128k_16,
 }

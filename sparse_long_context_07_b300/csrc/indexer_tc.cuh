@@ -309,7 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int wq = warp & 3;               // TMEM lane quarter of this warp
     const int et = threadIdx.x - 128 - e * 128;
     Walker wk;
-    Item item;
+    Item item{};
     int qi = 0, si = 0;
     bool ok = true;
     // after the item's last tile: wait until every epilogue thread has added
