@@ -324,8 +324,8 @@ typedef struct {
  * Copies and kernels overlap:
  *   - the key-side inputs (indexer k, k_scale and the latent cache) are
  *     copied in full first;
- *   - the query-side inputs are copied chunk by chunk on copy_in, in the
- *     query chunks dsa_forward uses;
+ *   - the query-side inputs are copied chunk by chunk on copy_in, in query
+ *     chunks of up to 4096 rows (fewer if the workspace holds fewer);
  *   - each chunk's kernels run on `stream` once its inputs have arrived;
  *   - its out / lse rows return on copy_out while later chunks compute.
  *

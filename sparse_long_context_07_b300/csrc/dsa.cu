@@ -475,6 +475,10 @@ FwdPlan plan_forward(int sms, const dsa_batch_t* b, const dsa_mla_t* m, int32_t 
 
 constexpr int64_t kPreferredChunk = 16384;
 constexpr int64_t kMinChunk = 64;
+// Query chunk of dsa_forward_streamed: the first chunk's inputs and the last
+// chunk's results are copied while no kernel runs, so smaller chunks than the
+// forward's shorten that fill and drain (copies, not kernels, bound that path).
+constexpr int64_t kStreamedChunk = 4096;
 
 int sms_for_sizing() {
   int dev = 0, sms = 148;
@@ -885,7 +889,7 @@ dsa_status_t dsa_forward_streamed(const dsa_batch_t* batch, const dsa_indexer_t*
   if (!ws || ws_bytes < mn.total)
     return fail(DSA_ERROR_INSUFFICIENT_WORKSPACE, "dsa_forward_streamed needs at least %zu bytes of workspace, got %zu",
                 mn.total, ws ? ws_bytes : 0);
-  int64_t lo = mn.chunk, hi = std::min<int64_t>(kPreferredChunk, batch->total_q);
+  int64_t lo = mn.chunk, hi = std::min<int64_t>(std::max(kStreamedChunk, mn.chunk), batch->total_q);
   if (plan_forward(dev->sms, batch, mla, k, hi).total <= ws_bytes) lo = hi;
   while (lo < hi) {
     const int64_t mid = (lo + hi + 1) / 2;
