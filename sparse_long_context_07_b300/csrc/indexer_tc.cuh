@@ -366,17 +366,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t ta = tmem + (static_cast<uint32_t>(wq * 32) << 16) + ab * kAccCols + e * kHeads;
           const int s = kt * kKeys + wq * 32 + lane;   // sequence-local key of this thread
           const float ks = (s <= plim && P.k_scale) ? __ldg(P.k_scale + item.kv0 + s) : 1.f;
-          uint32_t xa[32], xb[32];
-          tmem_ld32(ta, xa);
-          tmem_ld32(ta + 32, xb);
-          tmem_wait_ld();
-          tc_fence_before();
-          mbar_arrive(acc_empty(ab));      // accumulator read: the MMA may reuse it
           float2 acc[4];
 #pragma unroll
           for (int v = 0; v < 4; ++v) acc[v] = make_float2(0.f, 0.f);
-          reduce_chunk(xa, wsm, acc);
-          reduce_chunk(xb, wsm + 32, acc);
+          {
+            // the 64 head columns in two halves (32 registers of data live)
+            uint32_t x[32];
+            tmem_ld32(ta, x);
+            tmem_wait_ld();
+            reduce_chunk(x, wsm, acc);
+            tmem_ld32(ta + 32, x);
+            tmem_wait_ld();
+            tc_fence_before();
+            mbar_arrive(acc_empty(ab));      // accumulator read: the MMA may reuse it
+            reduce_chunk(x, wsm + 32, acc);
+          }
           const float2 tt = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
           if (s <= plim) {
             const float v = (tt.x + tt.y) * ks;
@@ -401,17 +405,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                             u * kHeads * item.g + te * kHeads;
         const int s = kt * kKeys + wq * 32 + lane;   // sequence-local key of this thread
         const float ks = (s <= plim && P.k_scale) ? __ldg(P.k_scale + item.kv0 + s) : 1.f;
-        uint32_t xa[32], xb[32];
-        tmem_ld32(ta, xa);
-        tmem_ld32(ta + 32, xb);
-        tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(acc_empty(ab));      // accumulator read: the MMA may reuse it
         float2 acc[4];
 #pragma unroll
         for (int v = 0; v < 4; ++v) acc[v] = make_float2(0.f, 0.f);
-        reduce_chunk(xa, wsm, acc);
-        reduce_chunk(xb, wsm + 32, acc);
+        {
+          // the 64 head columns in two halves (32 registers of data live)
+          uint32_t x[32];
+          tmem_ld32(ta, x);
+          tmem_wait_ld();
+          reduce_chunk(x, wsm, acc);
+          tmem_ld32(ta + 32, x);
+          tmem_wait_ld();
+          tc_fence_before();
+          mbar_arrive(acc_empty(ab));      // accumulator read: the MMA may reuse it
+          reduce_chunk(x, wsm + 32, acc);
+        }
         const float2 tt = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
         if (s <= plim) {
           const float v = (tt.x + tt.y) * ks;

@@ -121,3 +121,42 @@ def test_topk_cluster_and_row_kernels_agree():
         for r in (0, few // 2, few - 1):
             ref = oracle.topk_indices(S[r, :lens[r]].astype(np.float64), k)
             assert np.array_equal(outs[0][r].numpy(), ref), f"{kind} row {r}"
+
+
+@pytest.mark.parametrize("nbin", [8000, 8192, 8193, 12000])
+def test_topk_cluster_boundary_bin_sizes(nbin):
+    # decode rows whose k-th key sits in a top-11-bit bin of nbin keys
+    # (distinct values in [2, 2.5), one bin; the rest below): the cluster
+    # kernel keeps the bin's keys per warp and refines them across the CTAs
+    L, k = 60000, 2048
+    lens = [L, L - 5, 30001]
+    ld = L
+    batch = dsa.Batch(_cu([1] * len(lens)), _cu(lens), [1] * len(lens), lens)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(nbin)
+    scores = torch.randn((len(lens), ld), generator=g, device="cuda") * 0.3
+    for r, n in enumerate(lens):
+        m = min(nbin, n)
+        pos = torch.randperm(n, generator=g, device="cuda")[:m]
+        scores[r, pos] = 2.0 + 0.5 * torch.rand((m,), generator=g, device="cuda") * 0.999
+    # a few exact copies of one in-bin value: ties inside the refined bin
+    scores[0, 100:140] = scores[0, 99]
+    _check(batch, scores, ld, k, range(len(lens)), dict(enumerate(lens)))
+
+
+@pytest.mark.parametrize("nbin", [8000, 12000])
+def test_topk_cluster_boundary_bin_concentrated(nbin):
+    # nbin distinct keys of one top-11-bit bin in the first nbin positions of
+    # a 131072-candidate decode row: the first CTA's warps each hold about
+    # 1000 of them, more than a warp keeps, so the row takes the multi-pass
+    # path over the slices; the same keys spread over the row are kept per
+    # warp and refined across the cluster
+    n, k = 131072, 2048
+    batch = dsa.Batch(_cu([1, 1]), _cu([n, n]), [1, 1], [n, n])
+    g = torch.Generator(device="cuda")
+    g.manual_seed(77 + nbin)
+    scores = torch.randn((2, n), generator=g, device="cuda") * 0.3
+    vals = 2.0 + 0.5 * torch.rand((nbin,), generator=g, device="cuda") * 0.999
+    scores[0, :nbin] = vals
+    scores[1, torch.randperm(n, generator=g, device="cuda")[:nbin]] = vals
+    _check(batch, scores, n, k, range(2), {0: n, 1: n})
