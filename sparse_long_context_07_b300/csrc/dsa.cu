@@ -370,7 +370,7 @@ MlaPlan plan_dense_mla(int sms, int64_t rows, int32_t max_n, size_t ws_cap = SIZ
 dsa_status_t launch_sparse_mla(const DeviceInfo& dev, const dsa_batch_t* b, const dsa_mla_t* m,
                                const int32_t* idx, int32_t k, void* out, float* lse, void* ws,
                                size_t ws_bytes, int64_t r0, int64_t r1, cudaStream_t s, Tracer& tr,
-                               bool dense = false) {
+                               bool dense = false, bool pdl = false) {
   const int64_t rows = r1 - r0;
   if (rows <= 0) return DSA_SUCCESS;
   if (mla_is_tc(m)) {
@@ -414,7 +414,23 @@ dsa_status_t launch_sparse_mla(const DeviceInfo& dev, const dsa_batch_t* b, cons
     }
     const int64_t ctas = 2 * rows * plan.nsplit;
     if (ctas > 2147483647ll) return fail(DSA_ERROR_NOT_SUPPORTED, "too many query rows in one call");
-    dsa::mla_tc::mla_kernel<<<static_cast<unsigned>(ctas), dsa::mla_tc::kThreads, dsa::mla_tc::kSmemBytes, s>>>(tm_q, tm_out, P);
+    {
+      // pdl: launched as dependent on the kernel before it (the top-k), so its
+      // CTAs set up and load their queries while that kernel finishes; they
+      // wait for it before reading the index lists
+      cudaLaunchConfig_t cfg{};
+      cfg.gridDim = dim3(static_cast<unsigned>(ctas));
+      cfg.blockDim = dim3(dsa::mla_tc::kThreads);
+      cfg.dynamicSmemBytes = dsa::mla_tc::kSmemBytes;
+      cfg.stream = s;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      const cudaError_t e = cudaLaunchKernelEx(&cfg, dsa::mla_tc::mla_kernel, tm_q, tm_out, P);
+      if (e != cudaSuccess) return fail(DSA_ERROR_LAUNCH, "mla_tc launch failed: %s", cudaGetErrorString(e));
+    }
     DSA_TRY(check_launch("mla_tc"));
     tr.after(DSA_KERNEL_MLA_TC);
     if (plan.nsplit > 1) {
@@ -852,9 +868,12 @@ dsa_status_t dsa_forward_traced(const dsa_batch_t* batch, const dsa_indexer_t* i
     int32_t* idx = idx_out ? idx_out + r0 * k : idx_ws;
     DSA_TRY(launch_index_scores(*dev, batch, indexer, scores, plan.ld, r0, r1, stream, tr));
     DSA_TRY(launch_topk(*dev, batch, scores, plan.ld, k, idx, nullptr, r0, r1, stream, tr));
+    // (without a trace: each kernel's own time is not measured, so the
+    // attention kernel may overlap the end of the top-k)
     DSA_TRY(launch_sparse_mla(*dev, batch, mla, idx, k,
                               static_cast<char*>(out) + r0 * mla->n_heads * mla->d_v * static_cast<int64_t>(esz),
-                              lse ? lse + r0 * mla->n_heads : nullptr, mla_ws, plan.mla_bytes, r0, r1, stream, tr));
+                              lse ? lse + r0 * mla->n_heads : nullptr, mla_ws, plan.mla_bytes, r0, r1, stream, tr,
+                              false, trace == nullptr));
   }
   return DSA_SUCCESS;
 }

@@ -245,11 +245,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     if (half == 0 && P.prefetch_ahead > 0) {
-      // this token's queries and index list into L2 ahead of their loads,
-      // and the queries of the token that will likely run next on this SM
-      // pair (a wave of the grid later)
+      // this token's queries into L2 ahead of their loads, and the queries
+      // of the token that will likely run next on this SM pair (a wave of
+      // the grid later)
       if (nt > 0) prefetch_l2_bulk(P.q + row * kHeads * kDqk, kHeads * kDqk * 2);
-      if (nt > 0 && !P.dense && (P.k & 3) == 0) prefetch_l2_bulk(idx_row, P.k * 4);
       const int64_t nu = unit + P.prefetch_ahead;
       if (nu < P.units) prefetch_l2_bulk(P.q + (P.row0 + nu / P.nsplit) * kHeads * kDqk, kHeads * kDqk * 2);
     }
@@ -295,6 +294,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int gt = threadIdx.x - 128;
     const int i = gt >> 3, t8 = gt & 7;
     const int tr_own = kOwn * half + i, tr_peer = kOwn * static_cast<int>(peer) + i;
+    griddep_wait();   // the index lists may come from the kernel before this one
     int so_cur = sel_at(0, tr_own), sp_cur = sel_at(0, tr_peer);
     int so_next = sel_at(1, tr_own), sp_next = sel_at(1, tr_peer);
     const uint32_t swz = i * 128 + ((t8 ^ (i & 7)) << 4);
@@ -449,6 +449,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_arrive(qt_full);
     }
     float m_use = -INFINITY, l = 0.f;
+    griddep_wait();   // (the queries above are inputs of the call; the index lists are not)
     int sel_own = sr == 0 ? sel_at(0, kOwn * half + lane) : -1;
     for (int j = 0; j < nt; ++j) {
       const int xb = j & 1;

@@ -166,6 +166,7 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(
     int num_seqs, int64_t row0, const uint32_t* __restrict__ hist_in) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
+  griddep_launch_dependents();   // the attention kernel may set up while rows are selected
 
   const int tid = threadIdx.x;
   const int64_t r = row0 + blockIdx.x;
@@ -467,6 +468,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kCThreads, 4)
     int num_seqs, int64_t row0, const uint32_t* __restrict__ hist_in) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   CSmem& sm = *reinterpret_cast<CSmem*>(smem_raw);
+  griddep_launch_dependents();   // the attention kernel may set up while rows are selected
 
   const int tid = threadIdx.x, lane = tid & 31;
   const int c = static_cast<int>(cluster_ctarank());
