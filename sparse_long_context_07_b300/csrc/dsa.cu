@@ -10,9 +10,12 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <string>
+
+#include "nvtx3/nvToolsExt.h"
 
 #include "dsa.h"
 #include "common.cuh"
@@ -27,6 +30,30 @@
 namespace {
 
 thread_local std::string g_last_msg;
+
+// NVTX ranges (for timeline tools) around the entry points, the query chunks
+// of the forward and every kernel launch, when the environment sets
+// DSA_NVTX=1 (read once per process).  Without a tool attached a range is a
+// no-op call.
+bool nvtx_on() {
+  static const bool on = [] {
+    const char* v = std::getenv("DSA_NVTX");
+    return v != nullptr && v[0] == '1';
+  }();
+  return on;
+}
+
+struct NvtxRange {
+  const bool on;
+  explicit NvtxRange(const char* name) : on(nvtx_on()) {
+    if (on) nvtxRangePushA(name);
+  }
+  ~NvtxRange() {
+    if (on) nvtxRangePop();
+  }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 dsa_status_t fail(dsa_status_t st, const char* fmt, ...) {
   char buf[512];
@@ -233,6 +260,7 @@ dsa_status_t launch_index_scores(const DeviceInfo& dev, const dsa_batch_t* b, co
                                  Tracer& tr, uint32_t* hist = nullptr) {
   const int64_t rows = r1 - r0;
   if (rows <= 0) return DSA_SUCCESS;
+  NvtxRange nvtx("dsa: indexer");
   if (indexer_is_tc(ix)) {
     CUtensorMap tm_q, tm_k;
     DSA_TRY(encode_2d(&tm_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, ix->q, dsa::idx_tc::kDim,
@@ -298,6 +326,7 @@ dsa_status_t launch_index_scores(const DeviceInfo& dev, const dsa_batch_t* b, co
 dsa_status_t launch_topk(const DeviceInfo& dev, const dsa_batch_t* b, const float* scores, int64_t ld,
                          int32_t k, int32_t* idx, float* vals, int64_t r0, int64_t r1, cudaStream_t s,
                          Tracer& tr, const uint32_t* hist = nullptr) {
+  NvtxRange nvtx("dsa: top-k");
   if (r1 > r0 && (r1 - r0) * dsa::topk::kCluster <= 4 * static_cast<int64_t>(dev.sms)) {
     dsa::topk::topk_cluster_kernel<<<static_cast<unsigned>((r1 - r0) * dsa::topk::kCluster),
                                      dsa::topk::kCThreads, dsa::topk::kCSmemBytes, s>>>(
@@ -373,6 +402,7 @@ dsa_status_t launch_sparse_mla(const DeviceInfo& dev, const dsa_batch_t* b, cons
                                bool dense = false, bool pdl = false) {
   const int64_t rows = r1 - r0;
   if (rows <= 0) return DSA_SUCCESS;
+  NvtxRange nvtx(dense ? "dsa: dense attention" : "dsa: sparse attention");
   if (mla_is_tc(m)) {
     const MlaPlan plan = dense ? plan_dense_mla(dev.sms, rows, k, ws ? ws_bytes : 0)
                                : plan_mla(dev.sms, rows, k, ws ? ws_bytes : 0);
@@ -729,6 +759,7 @@ dsa_status_t dsa_sparse_mla_noalloc(const dsa_batch_t* batch, const dsa_mla_t* m
 
 dsa_status_t dsa_quantize_e4m3(const void* x, dsa_dtype_t x_dtype, int64_t groups, int32_t group_elems,
                                uint8_t* codes, float* scales, cudaStream_t stream) {
+  NvtxRange nvtx("dsa: quantize e4m3");
   if (groups < 0) return fail(DSA_ERROR_INVALID_VALUE, "groups must be >= 0");
   if (group_elems < 4 || group_elems > dsa::quant::kMaxGroup || group_elems % 4 != 0)
     return fail(DSA_ERROR_INVALID_VALUE, "group_elems must be a multiple of 4 in [4, %d]", dsa::quant::kMaxGroup);
@@ -775,6 +806,7 @@ dsa_status_t dsa_indexer_loss_workspace_size(const dsa_batch_t* batch, const dsa
 dsa_status_t dsa_indexer_warmup_loss(const dsa_batch_t* batch, const dsa_indexer_t* indexer, const dsa_mla_t* mla,
                                      float* loss_rows, float* dq, float* dk, float* dw, void* ws, size_t ws_bytes,
                                      cudaStream_t stream) {
+  NvtxRange nvtx("dsa: indexer warm-up loss");
   DSA_TRY(check_kl(batch, indexer, mla));
   if (batch->total_q == 0) return DSA_SUCCESS;
   if (!loss_rows || !dq || !dk || !dw || !aligned16(loss_rows) || !aligned16(dq) || !aligned16(dk) || !aligned16(dw))
@@ -832,6 +864,7 @@ dsa_status_t dsa_indexer_warmup_loss(const dsa_batch_t* batch, const dsa_indexer
 dsa_status_t dsa_forward_traced(const dsa_batch_t* batch, const dsa_indexer_t* indexer, const dsa_mla_t* mla,
                                 int32_t k, void* out, float* lse, int32_t* idx_out, void* ws, size_t ws_bytes,
                                 cudaStream_t stream, dsa_trace_t* trace) {
+  NvtxRange nvtx("dsa: forward");
   DSA_TRY(check_batch(batch));
   DSA_TRY(check_indexer(indexer, batch));
   DSA_TRY(check_mla(mla, batch));
@@ -865,6 +898,7 @@ dsa_status_t dsa_forward_traced(const dsa_batch_t* batch, const dsa_indexer_t* i
   DSA_TRY(tr.begin());
   for (int64_t r0 = 0; r0 < batch->total_q; r0 += plan.chunk) {
     const int64_t r1 = std::min<int64_t>(batch->total_q, r0 + plan.chunk);
+    NvtxRange chunk_range("dsa: query chunk");
     int32_t* idx = idx_out ? idx_out + r0 * k : idx_ws;
     DSA_TRY(launch_index_scores(*dev, batch, indexer, scores, plan.ld, r0, r1, stream, tr));
     DSA_TRY(launch_topk(*dev, batch, scores, plan.ld, k, idx, nullptr, r0, r1, stream, tr));
@@ -887,6 +921,7 @@ dsa_status_t dsa_forward_streamed(const dsa_batch_t* batch, const dsa_indexer_t*
                                   int32_t k, const dsa_host_inputs_t* host, void* out, float* lse, void* host_out,
                                   float* host_lse, void* ws, size_t ws_bytes, cudaStream_t stream,
                                   cudaStream_t copy_in, cudaStream_t copy_out) {
+  NvtxRange nvtx("dsa: forward (streamed)");
   DSA_TRY(check_batch(batch));
   DSA_TRY(check_indexer(indexer, batch));
   DSA_TRY(check_mla(mla, batch));
